@@ -1,0 +1,148 @@
+"""Pins of the oracle's plan replay.  A small instruction table is written by
+hand here from the documented record format (not by the library's planner);
+the replay must accept it, derive the per-step counter increments a reader can
+count by eye, and reject each planted mistake."""
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+
+NONE = 0xFFFFFFFF
+QKV, ATTN, OPROJ, GATEUP, DOWN, LM = 1, 2, 3, 4, 5, 6
+CFG = dict(n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=512,
+           vocab=256)
+
+
+def rec(op, layer=0, b=0, g=0, wait=(NONE, 0), sig=0, sig2=NONE, sig2_after=0, row0=0,
+        nrows=0, chunk=0, nchunk=0):
+    return struct.pack("<BBHHHIIIIIIIIIIQII", op, 0, layer, b, g, wait[0], wait[1], sig, sig2,
+                       sig2_after, row0, nrows, chunk, nchunk, 0, 0, 0, 0)
+
+
+def ctr(l, name, g=0):
+    """counter ids: per layer 8 counters, then lm_done = 16"""
+    base = 8 * l
+    return {"qkv": base + g, "arr": base + 2 + g, "attn": base + 4, "o": base + 5,
+            "gu": base + 6, "d": base + 7}[name]
+
+
+LM_DONE, NCTR = 16, 17
+
+
+def build(mut=None):
+    """Two layers, H 256, 4 q / 2 kv heads of 64, F 512, V 256, batch 1:
+    QKV 2 tiles per group (128 rows), attention 2 chunks per group, O/GU/D/LM
+    2 tiles each.  `mut(kind, l, k, fields)` may edit fields before packing."""
+    out = []
+
+    def add(kind, l, k, **f):
+        if mut:
+            mut(kind, l, k, f)
+        if f is not None and f.get("drop") is None:
+            out.append(f)
+
+    for l in range(2):
+        wait_x = (NONE, 0) if l == 0 else (ctr(l - 1, "d"), 2)
+        for g in range(2):
+            for t in range(2):
+                add("qkv", l, 2 * g + t, op=QKV, layer=l, g=g, wait=wait_x, sig=ctr(l, "qkv", g),
+                    row0=256 * g + 128 * t, nrows=128)
+        for g in range(2):
+            for c in range(2):
+                add("attn", l, 2 * g + c, op=ATTN, layer=l, b=0, g=g, wait=(ctr(l, "qkv", g), 2),
+                    sig=ctr(l, "arr", g), sig2=ctr(l, "attn"), sig2_after=2, chunk=c, nchunk=2)
+        for t in range(2):
+            add("o", l, t, op=OPROJ, layer=l, wait=(ctr(l, "attn"), 2), sig=ctr(l, "o"),
+                row0=128 * t, nrows=128)
+        for t in range(2):
+            add("gu", l, t, op=GATEUP, layer=l, wait=(ctr(l, "o"), 2), sig=ctr(l, "gu"),
+                row0=256 * t, nrows=256)
+        for t in range(2):
+            add("d", l, t, op=DOWN, layer=l, wait=(ctr(l, "gu"), 2), sig=ctr(l, "d"),
+                row0=128 * t, nrows=128)
+    for t in range(2):
+        add("lm", 0, t, op=LM, layer=0, wait=(ctr(1, "d"), 2), sig=LM_DONE, row0=128 * t,
+            nrows=128)
+    table = b"".join(rec(**{k: v for k, v in f.items()}) for f in out)
+    return np.frombuffer(table, dtype=np.uint8).copy(), len(out)
+
+
+def run(table, n, lists=(None, None), S=4):
+    return oracle.replay(table, n, NCTR, CFG, 1, S, *lists)
+
+
+def test_hand_table_is_accepted_with_countable_increments():
+    t, n = build()
+    assert n == 2 * (4 + 4 + 2 + 2 + 2) + 2
+    inc = run(t, n)
+    want = np.zeros(NCTR, np.uint32)
+    for l in range(2):
+        for g in range(2):
+            want[ctr(l, "qkv", g)] = 2
+            want[ctr(l, "arr", g)] = 2
+        want[ctr(l, "attn")] = 2  # one merge per (sequence, group)
+        for name in ("o", "gu", "d"):
+            want[ctr(l, name)] = 2
+    want[LM_DONE] = 2
+    assert np.array_equal(inc, want)
+
+
+@pytest.mark.parametrize("mut, why", [
+    (lambda k, l, i, f: f.update(wait=(f["wait"][0], 3)) if k == "o" else None, "waits for 3 signals"),
+    (lambda k, l, i, f: f.update(nrows=127) if (k, l, i) == ("d", 0, 1) else None, "not written"),
+    (lambda k, l, i, f: f.update(row0=0) if (k, l, i) == ("gu", 1, 1) else None, "written twice"),
+    (lambda k, l, i, f: f.update(wait=(ctr(0, "o"), 2)) if (k, l) == ("d", 0) else None, "may start before"),
+    (lambda k, l, i, f: f.update(wait=(ctr(1, "qkv", 0), 2)) if (k, l, i) == ("attn", 1, 2) else None, "may start before"),
+    (lambda k, l, i, f: f.update(wait=(ctr(0, "gu"), 2)) if (k, l) == ("qkv", 1) else None, "may start before"),
+    (lambda k, l, i, f: f.update(wait=(ctr(1, "attn"), 2)) if (k, l) == ("gu", 0) else None, "queued at or after"),
+    (lambda k, l, i, f: f.update(sig2_after=1) if k == "attn" else None, "attention fields"),
+    (lambda k, l, i, f: f.update(nchunk=3, sig2_after=3) if (k, l, i) == ("attn", 0, 0) else None, "chunk count"),
+    (lambda k, l, i, f: f.update(g=1) if (k, l, i) == ("qkv", 0, 0) else None, "outside group"),
+    (lambda k, l, i, f: f.update(wait=(NONE, 0)) if (k, l, i) == ("o", 0, 0) else None, "without a wait"),
+    (lambda k, l, i, f: f.update(sig=ctr(0, "arr", 1)) if (k, l, i) == ("o", 0, 0) else None, "arrival counter shared"),
+])
+def test_planted_mistakes_are_rejected(mut, why):
+    t, n = build(mut)
+    with pytest.raises(AssertionError, match=why):
+        run(t, n)
+
+
+def test_simulation_accepts_valid_and_finds_deadlock():
+    t, n = build()
+    for S, D in [(1, 1), (2, 2), (3, 8), (16, 4)]:
+        oracle.simulate(t, n, NCTR, S, D, seed=7, trials=20)
+    # an unreachable target: o-proj waits for 3 merges, only 2 ever happen
+    bad, n = build(lambda k, l, i, f: f.update(wait=(f["wait"][0], 3)) if k == "o" else None)
+    with pytest.raises(AssertionError, match="deadlock"):
+        oracle.simulate(bad, n, NCTR, 4, 2, seed=1, trials=3)
+
+
+def test_exhaustive_two_sm_search():
+    t, n = build()
+    states = oracle.explore(t, n, NCTR, 2)
+    assert states > n
+    # the first QKV tile waiting on the LM-head counter can never run, and
+    # everything after it depends on it: some interleaving must deadlock
+    bad, n2 = build(lambda k, l, i, f: f.update(wait=(LM_DONE, 2)) if (k, l, i) == ("qkv", 0, 0) else None)
+    with pytest.raises(AssertionError, match="deadlock"):
+        oracle.explore(bad, n2, NCTR, 1)
+
+
+def test_static_lists():
+    t, n = build()
+    S = 3
+    lists = [[i for i in range(n) if i % S == s] for s in range(S)]
+    off = np.cumsum([0] + [len(x) for x in lists]).astype(np.uint32)
+    idx = np.concatenate([np.array(x, np.uint32) for x in lists])
+    run(t, n, (off, idx), S=S)
+    oracle.simulate(t, n, NCTR, S, 2, seed=3, trials=10, list_off=off, list_idx=idx)
+    rev = idx.copy()
+    rev[0], rev[1] = rev[1], rev[0]
+    with pytest.raises(AssertionError, match="queue order"):
+        run(t, n, (off, rev), S=S)
+    short = off.copy()
+    short[-1] -= 1
+    with pytest.raises(AssertionError, match="cover"):
+        run(t, n, (short, idx), S=S)
