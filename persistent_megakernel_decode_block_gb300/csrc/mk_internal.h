@@ -1,0 +1,82 @@
+// mk_internal.h -- definitions shared by the planner, the host runtime and the
+// megakernel of libmk.so.  Nothing here is part of the public ABI (mk.h).
+#pragma once
+#include <stdint.h>
+
+#include "mk.h"
+
+namespace mk {
+
+// Block shape: warp 0 = loader, warp 1 = storer, warps 2.. = compute.
+// Roles after « 5 · La spécialisation des warps », §5.4 (loader, compute,
+// storer; the scheduler role is the loader's queue claim).
+constexpr int kComputeWarps = 14;  // 16 warps per block: 4 per SM sub-partition, 128 registers each
+constexpr int kThreads = 32 * (2 + kComputeWarps);
+constexpr int kFifo = 8;        // instructions a block may hold ahead of compute
+constexpr int kMaxBatch = 16;
+constexpr int kMaxQpg = 8;      // q heads per KV group
+constexpr int kMaxItems = 32;   // work items (row x slice) per GEMV instruction
+constexpr int kMaxChunks = 8;   // 256-column chunks per item (registers per lane / 8)
+constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
+constexpr int kMaxRing = 32;
+
+// control words (u32 index into the ctrl block)
+constexpr int kCtlStatus = 0, kCtlWhere = 1, kCtlAbort = 2, kCtlEpoch = 3;
+constexpr int kCtlExit = 32, kCtlQueue = 64, kCtlWords = 96;
+
+// run modes
+constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2;
+
+// GEMV geometry of one op: K input columns split into NS slices of SW
+// columns; an item = one weight row restricted to one slice (2*SW bytes);
+// ipp items are packed per shared-memory page; nch = SW/256 16-byte chunks
+// per lane.
+struct OpGeom {
+  uint32_t K, NS, SW, item_bytes, ipp, nch, rows_per_tile, wrows_per_tile;
+};
+
+struct KParams {
+  const mk_instr *instr;
+  uint32_t n_instr;
+  const uint32_t *list_off, *list_idx;
+  uint32_t *ctr, *ctrl, *exec;
+  const uint32_t *ctr_inc;  // signals per step of every counter
+  unsigned long long *trace;
+  const uint8_t *arena;
+  const uint16_t *embed;   // plain [V][H]
+  const uint16_t *norms;   // [L][2][H] then final [H]
+  uint16_t *kc, *vc;       // [L][B][nkv][max_ctx][d]
+  const int32_t *tokens, *positions;
+  float *logits;
+  float *x, *q, *attn, *h, *part;
+  const float *rope_cos, *rope_sin;  // [max_ctx][d/2]
+  OpGeom geom[8];
+  int32_t L, H, nq, nkv, d, F, V, B, max_ctx, qpg;
+  int32_t nchunk, attn_chunk;
+  float eps, attn_scale;
+  int32_t n_wait, mode;
+  uint32_t range_first, range_count, n_blocks, flags;
+  uint64_t timeout_ns;
+  // dynamic shared-memory layout (byte offsets)
+  uint32_t ring_pages, page_bytes;
+  uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,
+      off_rope, off_normr, off_misc, smem_total;
+};
+
+// per FIFO slot metadata written by the loader
+struct SlotMeta {
+  uint32_t idx, seq0, npages, pad;
+  unsigned long long t_claim, t_ready;
+};
+
+#ifdef __CUDACC__
+cudaError_t set_megakernel_smem(uint32_t bytes);
+cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
+                              cudaStream_t stream);
+cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream);
+cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map, uint32_t nrows,
+                          const OpGeom &g, uint32_t page, uint64_t tile_stride,
+                          cudaStream_t stream);
+#endif
+
+}  // namespace mk

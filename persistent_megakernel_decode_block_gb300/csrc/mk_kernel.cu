@@ -1,0 +1,1116 @@
+// mk_kernel.cu -- the persistent decode megakernel (sm_103a).
+//
+// One launch runs a whole decoder forward pass (« 2 · Définition et
+// généalogie », §2.1).  The grid holds one resident block per SM (§2.6,
+// "1. La persistance"); each block interprets instructions taken from a
+// global work queue or from its own list (§2.4, persistent-threads loop;
+// §2.6, "2. Le dispatch d'instructions" and "5. L'ordonnancement").  Inside
+// a block the warps are specialised (« 5 · La spécialisation des warps »,
+// §5.2 and §5.4):
+//   warp 0       loader : claims instructions, streams their weight pages
+//                (or KV-cache rows) with bulk async copies into a ring of
+//                shared-memory pages tracked by full/empty mbarriers (§5.2's
+//                producer/consumer ring; §2.6, "4. L'allocateur de mémoire
+//                partagée"), and runs ahead across dependency waits (§5.4:
+//                load the next op's weights while the current one finishes).
+//   warp 1       storer : epilogues (RoPE, KV append, residual add, SiLU,
+//                attention merge), global stores, then the release of the
+//                instruction's dependency counter (§2.6, "3. Les compteurs").
+//   warps 2..15  compute: wait on the instruction's counter (acquire), then
+//                bf16 GEMV with fp32 accumulation from the ring pages, or a
+//                split-KV attention chunk.
+// Every wait is bounded by %globaltimer; on expiry the block latches
+// MK_ERR_TIMEOUT, raises a global abort flag that every other wait polls,
+// waits for its own copies in flight and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+#define DEVI __device__ __forceinline__
+
+// ---------------------------------------------------------------- PTX ----
+DEVI uint32_t saddr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+DEVI void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+DEVI void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+DEVI void mbar_arrive_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes)
+               : "memory");
+}
+DEVI bool mbar_try_wait(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+DEVI uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// bulk async copy global -> this CTA's shared memory, completion counted in bytes on `bar`
+DEVI void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(saddr(dst)),
+      "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol)
+      : "memory");
+}
+DEVI uint32_t ld_acquire(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DEVI uint32_t ld_relaxed(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DEVI void red_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DEVI uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+DEVI void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+DEVI uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+DEVI uint32_t smid() {
+  uint32_t s;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+  return s;
+}
+DEVI float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+DEVI float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+DEVI float bf1(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+DEVI uint16_t to_bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+DEVI float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+DEVI float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// ------------------------------------------------------- shared state ----
+struct Smem {
+  uint8_t *ring;
+  uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar;
+  mk_instr *fifo;
+  SlotMeta *meta;
+  float *res, *att_s, *opart, *lpart, *rope, *normr;
+  uint32_t *sat;
+  int32_t *pos, *tok;
+  volatile int *misc;  // [0] bail, [1] bad input
+};
+
+DEVI Smem make_smem(const KParams &P, uint8_t *base) {
+  Smem S;
+  S.ring = base;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(base + P.off_bars);
+  const uint32_t E = P.ring_pages;
+  S.full = bars;
+  S.empty = bars + E;
+  S.ifull = bars + 2 * E;
+  S.iempty = S.ifull + kFifo;
+  S.rdy = S.iempty + kFifo;
+  S.done = S.rdy + kFifo;
+  S.attbar = S.done + kFifo;
+  S.xbar = S.attbar + 1;
+  S.fifo = reinterpret_cast<mk_instr *>(base + P.off_fifo);
+  S.meta = reinterpret_cast<SlotMeta *>(base + P.off_meta);
+  S.res = reinterpret_cast<float *>(base + P.off_res);
+  S.att_s = reinterpret_cast<float *>(base + P.off_att);
+  S.opart = S.att_s + P.qpg * P.attn_chunk;
+  S.lpart = S.opart + kComputeWarps * P.d;
+  S.sat = reinterpret_cast<uint32_t *>(base + P.off_sat);
+  S.pos = reinterpret_cast<int32_t *>(base + P.off_pos);
+  S.tok = S.pos + kMaxBatch;
+  S.rope = reinterpret_cast<float *>(base + P.off_rope);
+  S.normr = reinterpret_cast<float *>(base + P.off_normr);
+  S.misc = reinterpret_cast<volatile int *>(base + P.off_misc);
+  return S;
+}
+
+// where-codes for the latched error: role << 28 | instruction index
+constexpr uint32_t kWhereLoader = 1u << 28, kWhereCompute = 2u << 28, kWhereStorer = 3u << 28,
+                   kWherePoll = 4u << 28, kWhereDrain = 5u << 28;
+
+DEVI void raise_error(const KParams &P, int code, uint32_t where, bool abort_all) {
+  atomicCAS(P.ctrl + kCtlStatus, 0u, (uint32_t)code);
+  atomicCAS(P.ctrl + kCtlWhere, 0u, where | 0x80000000u);
+  if (abort_all) atomicExch(P.ctrl + kCtlAbort, 1u);
+}
+
+// One thread: stop if the block bails, the grid aborts, or the limit passed.
+DEVI bool should_stop(const KParams &P, const Smem &S, uint64_t t0, uint32_t &n, uint32_t where) {
+  if (S.misc[0]) return true;
+  if ((++n & 7u) == 0) {
+    if (ld_relaxed(P.ctrl + kCtlAbort)) {
+      S.misc[0] = 1;
+      return true;
+    }
+    if (gtimer() - t0 > P.timeout_ns) {
+      raise_error(P, MK_ERR_TIMEOUT, where, true);
+      S.misc[0] = 1;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Single-thread bounded wait on an mbarrier phase.
+DEVI bool thread_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity,
+                      uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity))
+    if (should_stop(P, S, t0, n, where)) return false;
+  return true;
+}
+
+// Whole-warp bounded wait: every lane observes the phase itself (acquire);
+// lane 0 decides on bailing and broadcasts it.
+DEVI bool warp_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity,
+                    uint32_t where) {
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = gtimer();
+  uint32_t n = 0;
+  while (true) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) stop = should_stop(P, S, t0, n, where);
+    if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+  }
+}
+
+// ----------------------------------------------------- attention range ----
+// Chunk c of nch covers positions [p0, p1) of 0..pos: every chunk has the
+// same length (a multiple of 16), the last ones may be short or empty.
+DEVI void attn_range(int pos, int nch, int c, int &p0, int &p1) {
+  const int sb = (((pos + 1) + nch - 1) / nch + 15) & ~15;
+  p0 = c * sb;
+  p1 = min(p0 + sb, pos + 1);
+  if (p1 < p0) p1 = p0;
+}
+
+DEVI size_t kv_row(const KParams &P, int l, int b, int g, int p) {
+  return ((((size_t)l * P.B + b) * P.nkv + g) * P.max_ctx + p) * P.d;
+}
+
+// pages the loader streams for an instruction
+DEVI uint32_t n_pages(const KParams &P, const Smem &S, const mk_instr &in) {
+  if (in.op != MK_OP_ATTN) return in.npages;
+  int p0, p1;
+  const int pos = S.pos[in.b];
+  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  const int n_old = max(0, min(p1, pos) - p0);
+  const int rpp = P.page_bytes / (P.d * 2);
+  return 2u * (uint32_t)((n_old + rpp - 1) / rpp);
+}
+
+DEVI void page_src(const KParams &P, const Smem &S, const mk_instr &in, uint32_t p,
+                   uint32_t np, const void *&src, uint32_t &bytes) {
+  if (in.op != MK_OP_ATTN) {
+    const OpGeom &G = P.geom[in.op];
+    const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+    const uint32_t items = wrows * G.NS;
+    const uint32_t n = min(G.ipp, items - p * G.ipp);
+    src = P.arena + in.wofs + (uint64_t)p * P.page_bytes;
+    bytes = n * G.item_bytes;
+    return;
+  }
+  int p0, p1;
+  const int pos = S.pos[in.b];
+  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  const int n_old = max(0, min(p1, pos) - p0);
+  const int rpp = P.page_bytes / (P.d * 2);
+  const uint32_t npk = np / 2;
+  const bool is_v = p >= npk;
+  const int pp = (int)(is_v ? p - npk : p);
+  const int r0 = pp * rpp, rows = min(rpp, n_old - r0);
+  const uint16_t *base = (is_v ? P.vc : P.kc) + kv_row(P, in.layer, in.b, in.g, p0 + r0);
+  src = base;
+  bytes = (uint32_t)rows * P.d * 2;
+}
+
+// --------------------------------------------------------------- loader ----
+DEVI void drain_copies(const KParams &P, const Smem &S, uint32_t seq) {
+  const uint32_t E = P.ring_pages;
+  const uint32_t first = seq > E ? seq - E : 0;
+  for (uint32_t s = first; s < seq; ++s) {
+    uint64_t *bar = &S.full[s % E];
+    const uint32_t par = (s / E) & 1u;
+    const uint64_t t0 = gtimer();
+    while (!mbar_try_wait(bar, par))
+      if (gtimer() - t0 > 200000000ull) {  // 200 ms: a bulk copy never takes that long
+        raise_error(P, MK_ERR_TIMEOUT, kWhereDrain | s, true);
+        break;
+      }
+  }
+}
+
+DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
+  const uint64_t pol = policy_evict_first();
+  const uint32_t N = P.n_instr, E = P.ring_pages, PG = P.page_bytes;
+  const uint32_t qbase = epoch * (N + P.n_blocks);
+  uint32_t list_k = 0, list_end = 0, range_taken = 0;
+  if (P.mode == kModeStatic) {
+    list_k = P.list_off[blockIdx.x];
+    list_end = P.list_off[blockIdx.x + 1];
+  }
+  auto claim = [&]() -> uint32_t {
+    if (P.mode == kModeDynamic) return atomicAdd(P.ctrl + kCtlQueue, 1u) - qbase;
+    if (P.mode == kModeStatic) return list_k < list_end ? P.list_idx[list_k++] : N;
+    const uint32_t r = range_taken ? N : P.range_first + blockIdx.x;
+    range_taken = 1;
+    return r;
+  };
+  uint32_t seq = 0;
+  bool ok = true;
+  uint32_t next = claim();
+  for (uint32_t fs = 0; ok; ++fs) {
+    const uint32_t f = fs % kFifo, k = fs / kFifo;
+    if (k > 0 && !thread_wait(P, S, &S.iempty[f], (k - 1) & 1u, kWhereLoader | next)) {
+      ok = false;
+      break;
+    }
+    const uint32_t idx = next;
+    if (idx >= N) {
+      S.fifo[f].op = MK_OP_END;
+      S.meta[f].idx = N;
+      mbar_arrive(&S.ifull[f]);
+      break;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(P.instr + idx);
+    uint4 *dst = reinterpret_cast<uint4 *>(&S.fifo[f]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = __ldg(src + i);
+    const mk_instr in = S.fifo[f];
+    next = claim();  // the next claim overlaps this instruction's copies
+    const uint32_t np = n_pages(P, S, in);
+    SlotMeta &m = S.meta[f];
+    m.idx = idx;
+    m.seq0 = seq;
+    m.npages = np;
+    m.t_claim = (P.flags & MK_FLAG_TRACE) ? gtimer() : 0ull;
+    mbar_arrive(&S.ifull[f]);
+    for (uint32_t p = 0; p < np; ++p) {
+      const uint32_t slot = seq % E, kk = seq / E;
+      if (kk > 0 && !thread_wait(P, S, &S.empty[slot], (kk - 1) & 1u, kWhereLoader | idx)) {
+        ok = false;
+        break;
+      }
+      const void *gsrc;
+      uint32_t bytes;
+      page_src(P, S, in, p, np, gsrc, bytes);
+      mbar_arrive_expect_tx(&S.full[slot], bytes);
+      bulk_g2s(S.ring + (size_t)slot * PG, gsrc, bytes, &S.full[slot], pol);
+      ++seq;
+    }
+  }
+  if (!ok) drain_copies(P, S, seq);
+}
+
+// -------------------------------------------------------------- compute ----
+// Wait for the instruction's input counter (one thread).  `sat` caches the
+// last satisfied absolute target per waited counter for this launch.
+DEVI bool poll_counter(const KParams &P, const Smem &S, const mk_instr &in, uint32_t epoch,
+                       uint32_t idx) {
+  if (P.mode == kModeRange || in.wait_ctr == MK_NO_COUNTER) return true;
+  const uint32_t c = in.wait_ctr;
+  // counters are never reset: this step's target sits on top of the
+  // epoch * (signals per step) the counter received in earlier steps
+  const uint32_t target = epoch * __ldg(P.ctr_inc + c) + in.wait_tgt;
+  const bool cacheable = c < (uint32_t)P.n_wait;
+  if (cacheable && S.sat[c] != 0 && (int32_t)((S.sat[c] - 1u) - target) >= 0) return true;
+  const uint32_t *p = P.ctr + (size_t)c * kCtrStride;
+  bool ok = (int32_t)(ld_acquire(p) - target) >= 0;
+  if (!ok) {
+    const uint64_t t0 = gtimer();
+    uint32_t n = 0;
+    while (true) {
+      __nanosleep(20);
+      if ((int32_t)(ld_acquire(p) - target) >= 0) {
+        ok = true;
+        break;
+      }
+      if (should_stop(P, S, t0, n, kWherePoll | idx)) return false;
+    }
+  }
+  if (cacheable) S.sat[c] = target + 1u;
+  return true;
+}
+
+struct XCache {
+  float v[kMaxChunks][8];
+};
+
+DEVI const uint16_t *gain_of(const KParams &P, int op, int layer) {
+  if (op == MK_OP_QKV) return P.norms + (size_t)(2 * layer) * P.H;
+  if (op == MK_OP_GATEUP) return P.norms + (size_t)(2 * layer + 1) * P.H;
+  if (op == MK_OP_LMHEAD) return P.norms + (size_t)(2 * P.L) * P.H;
+  return nullptr;
+}
+
+// 8 consecutive input values of sequence b at column col
+DEVI void load8(const KParams &P, const Smem &S, int op, int emb, int b, int col, float (&v)[8]) {
+  if (emb) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(P.embed + (size_t)S.tok[b] * P.H + col));
+    v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+    v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+    return;
+  }
+  const float *src;
+  if (op == MK_OP_OPROJ) src = P.attn + (size_t)b * P.nq * P.d;
+  else if (op == MK_OP_DOWN) src = P.h + (size_t)b * P.F;
+  else src = P.x + (size_t)b * P.H;
+  const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + col));
+  const float4 c = __ldcg(reinterpret_cast<const float4 *>(src + col + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+}
+
+DEVI void load_gain8(const uint16_t *g, int col, float (&v)[8]) {
+  const uint4 w = __ldg(reinterpret_cast<const uint4 *>(g + col));
+  v[0] = bf_lo(w.x); v[1] = bf_hi(w.x); v[2] = bf_lo(w.y); v[3] = bf_hi(w.y);
+  v[4] = bf_lo(w.z); v[5] = bf_hi(w.z); v[6] = bf_lo(w.w); v[7] = bf_hi(w.w);
+}
+
+// Batch 1: the warp's input slice, normalised and scaled by the gains, kept
+// in registers for as long as consecutive instructions share the input.
+DEVI void load_input_b1(const KParams &P, const Smem &S, const mk_instr &in, uint32_t s,
+                        int lane, XCache &X) {
+  const OpGeom &G = P.geom[in.op];
+  const int emb = in.op == MK_OP_QKV && (in.flags & 1);
+  const uint16_t *gain = gain_of(P, in.op, in.layer);
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j)
+    if (j < (int)G.nch) {
+      load8(P, S, in.op, emb, 0, s * G.SW + j * 256 + lane * 8, X.v[j]);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) ss = fmaf(X.v[j][t], X.v[j][t], ss);
+    }
+  if (gain) {
+    for (uint32_t s2 = 0; s2 < G.NS; ++s2) {
+      if (s2 == s) continue;
+      for (uint32_t j = 0; j < G.nch; ++j) {
+        float t8[8];
+        load8(P, S, in.op, emb, 0, s2 * G.SW + j * 256 + lane * 8, t8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) ss = fmaf(t8[t], t8[t], ss);
+      }
+    }
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)G.K + P.eps);
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j)
+      if (j < (int)G.nch) {
+        float g8[8];
+        load_gain8(gain, s * G.SW + j * 256 + lane * 8, g8);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) X.v[j][t] *= r * g8[t];
+      }
+  }
+}
+
+DEVI float dot_item_b1(const uint8_t *item, const XCache &X, int nch, int lane) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j)
+    if (j < nch) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(item + j * 512 + lane * 16);
+      a0 = fmaf(bf_lo(w.x), X.v[j][0], a0);
+      a1 = fmaf(bf_hi(w.x), X.v[j][1], a1);
+      a2 = fmaf(bf_lo(w.y), X.v[j][2], a2);
+      a3 = fmaf(bf_hi(w.y), X.v[j][3], a3);
+      a0 = fmaf(bf_lo(w.z), X.v[j][4], a0);
+      a1 = fmaf(bf_hi(w.z), X.v[j][5], a1);
+      a2 = fmaf(bf_lo(w.w), X.v[j][6], a2);
+      a3 = fmaf(bf_hi(w.w), X.v[j][7], a3);
+    }
+  return (a0 + a1) + (a2 + a3);
+}
+
+// Batch > 1: per-sequence 1/rms at every change of input, shared through
+// shared memory (double-buffered by the change count).
+DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int cw, int lane,
+                       uint32_t &xbar_uses, float *normr) {
+  const OpGeom &G = P.geom[in.op];
+  const int emb = in.op == MK_OP_QKV && (in.flags & 1);
+  const bool norm = gain_of(P, in.op, in.layer) != nullptr;
+  if (cw < P.B) {
+    float r = 1.f;
+    if (norm) {
+      float ss = 0.f;
+      for (uint32_t c = lane * 8; c < G.K; c += 256) {
+        float v[8];
+        load8(P, S, in.op, emb, cw, c, v);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
+      }
+      ss = warp_sum(ss);
+      r = rsqrtf(ss / (float)G.K + P.eps);
+    }
+    if (lane == 0) normr[cw] = r;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(S.xbar);
+  const bool ok = warp_wait(P, S, S.xbar, xbar_uses & 1u, kWhereCompute);
+  ++xbar_uses;
+  return ok;
+}
+
+// Batch-1 GEMV of one instruction; X holds the normalised input slice when
+// xkey matches the instruction's input.
+DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
+                  float *res, int cw, int lane, XCache &X, uint32_t &xkey) {
+  const OpGeom &G = P.geom[in.op];
+  const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+  const uint32_t items = wrows * G.NS;
+  const uint32_t A = G.NS * (kComputeWarps / G.NS);
+  const bool active = (uint32_t)cw < A;
+  const uint32_t s = cw % G.NS;
+  const uint32_t key = ((uint32_t)in.op << 24) | ((uint32_t)(in.flags & 1) << 23) | in.layer;
+  if (key != xkey) {
+    if (active) load_input_b1(P, S, in, s, lane, X);
+    xkey = key;
+  }
+  const uint32_t E = P.ring_pages;
+  uint32_t item = cw;
+  for (uint32_t p = 0; p < meta.npages; ++p) {
+    const uint32_t seq = meta.seq0 + p, slot = seq % E;
+    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    const uint8_t *page = S.ring + (size_t)slot * P.page_bytes;
+    const uint32_t it_end = min(items, (p + 1) * G.ipp);
+    for (; active && item < it_end; item += A) {
+      const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
+      const float acc = warp_sum(dot_item_b1(ip, X, G.nch, lane));
+      if (lane == 0) res[item] = acc;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  return true;
+}
+
+// Batch > 1 GEMV of one instruction: every item is dotted with the B input
+// rows (read through L2), the gains folded into the weights and 1/rms
+// applied at the end.
+__device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
+                  float *res, int cw, int lane, uint32_t &xkey, uint32_t &xbar_uses,
+                  uint32_t &key_changes) {
+  const OpGeom &G = P.geom[in.op];
+  const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+  const uint32_t items = wrows * G.NS;
+  const uint32_t A = G.NS * (kComputeWarps / G.NS);
+  const bool active = (uint32_t)cw < A;
+  const uint32_t s = cw % G.NS;
+  const uint32_t key = ((uint32_t)in.op << 24) | ((uint32_t)(in.flags & 1) << 23) | in.layer;
+  const int B = P.B;
+  if (key != xkey) {
+    ++key_changes;
+    if (!norm_factors(P, S, in, cw, lane, xbar_uses, S.normr + (key_changes & 1u) * kMaxBatch))
+      return false;
+    xkey = key;
+  }
+  const float *normr = S.normr + (key_changes & 1u) * kMaxBatch;
+  const int emb = in.op == MK_OP_QKV && (in.flags & 1);
+  const uint16_t *gain = gain_of(P, in.op, in.layer);
+  const uint32_t E = P.ring_pages;
+  uint32_t item = cw;
+  for (uint32_t p = 0; p < meta.npages; ++p) {
+    const uint32_t seq = meta.seq0 + p, slot = seq % E;
+    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    const uint8_t *page = S.ring + (size_t)slot * P.page_bytes;
+    const uint32_t it_end = min(items, (p + 1) * G.ipp);
+    for (; active && item < it_end; item += A) {
+      const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
+      float acc[kMaxBatch];
+#pragma unroll
+      for (int b = 0; b < kMaxBatch; ++b) acc[b] = 0.f;
+      for (uint32_t j = 0; j < G.nch; ++j) {
+        const int col = s * G.SW + j * 256 + lane * 8;
+        const uint4 w = *reinterpret_cast<const uint4 *>(ip + j * 512 + lane * 16);
+        float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                       bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+        if (gain) {
+          float g8[8];
+          load_gain8(gain, col, g8);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) wf[t] *= g8[t];
+        }
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b)
+          if (b < B) {
+            float v[8];
+            load8(P, S, in.op, emb, b, col, v);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc[b] = fmaf(wf[t], v[t], acc[b]);
+          }
+      }
+#pragma unroll
+      for (int b = 0; b < kMaxBatch; ++b)
+        if (b < B) {
+          const float a = warp_sum(acc[b]) * normr[b];
+          if (lane == 0) res[item * B + b] = a;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  return true;
+}
+
+// Barrier of the compute warps on an mbarrier (bounded).
+DEVI bool compute_sync(const KParams &P, const Smem &S, uint64_t *bar, uint32_t &uses, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = warp_wait(P, S, bar, uses & 1u, kWhereCompute);
+  ++uses;
+  return ok;
+}
+
+// One split-KV attention chunk for the QPG query heads of group g of
+// sequence b: scores q.k/sqrt(d) over the chunk's positions, then the
+// chunk's max m, denominator l = sum exp(s - m) and unnormalised output
+// sum exp(s - m) v, written to the slot's result area as {m[QPG], l[QPG],
+// o[QPG][D]}.  Keys/values of positions below p_b come from the ring
+// pages; the one at p_b (written this step) from global memory.
+template <int D, int QPG>
+__device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
+                     float *res, int cw, int lane, uint32_t &att_uses) {
+  constexpr int LPP = D / 8;       // lanes per key row (16 bytes each)
+  constexpr int PPW = 32 / LPP;    // key rows per warp step
+  constexpr int T = kComputeWarps * PPW;
+  constexpr int DPL = D / 32;      // value dims per lane
+  const int b = in.b, g = in.g, pos = S.pos[b];
+  int p0, p1;
+  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  const int n_tot = p1 - p0;
+  const int n_old = max(0, min(p1, pos) - p0);
+  const int rpp = P.page_bytes / (D * 2);
+  const int npk = (n_old + rpp - 1) / rpp;
+  const int CH = P.attn_chunk;
+  const uint32_t E = P.ring_pages;
+  float *s_buf = S.att_s;
+  const int part = lane % LPP, t = cw * PPW + lane / LPP;
+  const float scale = P.attn_scale;
+
+  float q[QPG][8];
+  {
+    const float *qb = P.q + ((size_t)b * P.nq + (size_t)g * QPG) * D + part * 8;
+#pragma unroll
+    for (int h = 0; h < QPG; ++h) {
+      const float4 a = __ldcg(reinterpret_cast<const float4 *>(qb + h * D));
+      const float4 c = __ldcg(reinterpret_cast<const float4 *>(qb + h * D + 4));
+      q[h][0] = a.x; q[h][1] = a.y; q[h][2] = a.z; q[h][3] = a.w;
+      q[h][4] = c.x; q[h][5] = c.y; q[h][6] = c.z; q[h][7] = c.w;
+    }
+  }
+  auto score_rows = [&](const uint8_t *rows, const uint16_t *grow, int a, int e) {
+    for (int jj = a - (a % T); jj < e; jj += T) {
+      const int j = jj + t;
+      const bool valid = j >= a && j < e;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+        if (rows) w = *reinterpret_cast<const uint4 *>(rows + (size_t)(j - a) * D * 2 + part * 16);
+        else w = __ldcg(reinterpret_cast<const uint4 *>(grow + part * 8));
+      }
+      const float k8[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                           bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+#pragma unroll
+      for (int h = 0; h < QPG; ++h) {
+        float dsum = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dsum = fmaf(q[h][u], k8[u], dsum);
+#pragma unroll
+        for (int o = LPP / 2; o; o >>= 1) dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
+        if (valid && part == 0) s_buf[h * CH + j] = dsum * scale;
+      }
+    }
+  };
+  // scores: K pages, then the new key
+  for (int p = 0; p < npk; ++p) {
+    const uint32_t seq = meta.seq0 + p, slot = seq % E;
+    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    const int a = p * rpp, e = min(n_old, a + rpp);
+    score_rows(S.ring + (size_t)slot * P.page_bytes, nullptr, a, e);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  if (n_tot > n_old) score_rows(nullptr, P.kc + kv_row(P, in.layer, b, g, pos), n_old, n_tot);
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+
+  // per-head maximum (every warp computes the same values)
+  float m[QPG];
+#pragma unroll
+  for (int h = 0; h < QPG; ++h) {
+    float mx = -INFINITY;
+    for (int j = lane; j < n_tot; j += 32) mx = fmaxf(mx, s_buf[h * CH + j]);
+    m[h] = warp_max(mx);
+  }
+  // p = exp(s - m) against V rows: warp cw -> head hh = cw % QPG, position
+  // subset qs = cw / QPG of the nqs(hh) warps that serve that head
+  const int hh = cw % QPG, qs = cw / QPG;
+  const int NQS = (kComputeWarps - 1 - hh) / QPG + 1;
+  float o[DPL];
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
+  float lsum = 0.f;
+  float mh = m[0];
+#pragma unroll
+  for (int h = 1; h < QPG; ++h)
+    if (h == hh) mh = m[h];
+  auto pv_rows = [&](const uint8_t *rows, const uint16_t *grow, int a, int e) {
+    int j = a + ((qs - a % NQS) % NQS + NQS) % NQS;
+    for (; j < e; j += NQS) {
+      const float pj = __expf(s_buf[hh * CH + j] - mh);
+      lsum += pj;
+      if constexpr (DPL == 2) {
+        uint32_t w;
+        if (rows) w = *reinterpret_cast<const uint32_t *>(rows + (size_t)(j - a) * D * 2 + lane * 4);
+        else w = __ldcg(reinterpret_cast<const unsigned int *>(grow + lane * 2));
+        o[0] = fmaf(pj, bf_lo(w), o[0]);
+        o[1] = fmaf(pj, bf_hi(w), o[1]);
+      } else {
+        uint2 w;
+        if (rows) w = *reinterpret_cast<const uint2 *>(rows + (size_t)(j - a) * D * 2 + lane * 8);
+        else w = __ldcg(reinterpret_cast<const uint2 *>(grow + lane * 4));
+        o[0] = fmaf(pj, bf_lo(w.x), o[0]);
+        o[1] = fmaf(pj, bf_hi(w.x), o[1]);
+        o[2] = fmaf(pj, bf_lo(w.y), o[2]);
+        o[3] = fmaf(pj, bf_hi(w.y), o[3]);
+      }
+    }
+  };
+  for (int p = 0; p < npk; ++p) {
+    const uint32_t seq = meta.seq0 + npk + p, slot = seq % E;
+    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    const int a = p * rpp, e = min(n_old, a + rpp);
+    pv_rows(S.ring + (size_t)slot * P.page_bytes, nullptr, a, e);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  if (n_tot > n_old) pv_rows(nullptr, P.vc + kv_row(P, in.layer, b, g, pos), n_old, n_tot);
+#pragma unroll
+  for (int k = 0; k < DPL; ++k) S.opart[cw * D + lane * DPL + k] = o[k];
+  if (lane == 0) S.lpart[cw] = lsum;
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (cw < QPG) {
+    const int h = cw, nh = (kComputeWarps - 1 - h) / QPG + 1;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      float acc = 0.f;
+      for (int r = 0; r < nh; ++r) acc += S.opart[(h + r * QPG) * D + lane * DPL + k];
+      res[2 * QPG + h * D + lane * DPL + k] = acc;
+    }
+    if (lane == 0) {
+      float l = 0.f, mv = m[0];
+      for (int r = 0; r < nh; ++r) l += S.lpart[h + r * QPG];
+#pragma unroll
+      for (int hq = 1; hq < QPG; ++hq)
+        if (hq == h) mv = m[hq];
+      res[h] = mv;
+      res[QPG + h] = l;
+    }
+  }
+  return true;
+}
+
+DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
+                        const SlotMeta &meta, float *res, int cw, int lane, uint32_t &att_uses) {
+  if (P.d == 64) {
+    switch (P.qpg) {
+      case 1: return attn_chunk<64, 1>(P, S, in, meta, res, cw, lane, att_uses);
+      case 2: return attn_chunk<64, 2>(P, S, in, meta, res, cw, lane, att_uses);
+      case 4: return attn_chunk<64, 4>(P, S, in, meta, res, cw, lane, att_uses);
+      default: return attn_chunk<64, 8>(P, S, in, meta, res, cw, lane, att_uses);
+    }
+  }
+  switch (P.qpg) {
+    case 1: return attn_chunk<128, 1>(P, S, in, meta, res, cw, lane, att_uses);
+    case 2: return attn_chunk<128, 2>(P, S, in, meta, res, cw, lane, att_uses);
+    case 4: return attn_chunk<128, 4>(P, S, in, meta, res, cw, lane, att_uses);
+    default: return attn_chunk<128, 8>(P, S, in, meta, res, cw, lane, att_uses);
+  }
+}
+
+// Wait for FIFO entry fs (idempotent: may be called again for the same
+// entry).  The entry stays in shared memory, read in place, until the
+// storer releases the slot.
+DEVI bool next_entry(const KParams &P, const Smem &S, uint32_t fs) {
+  const uint32_t f = fs % kFifo, k = fs / kFifo;
+  return warp_wait(P, S, &S.ifull[f], k & 1u, kWhereCompute);
+}
+
+// Dependency wait of entry fs: compute warp 0 polls the counter, the others
+// wait on the slot's ready barrier.
+DEVI bool ready_entry(const KParams &P, const Smem &S, uint32_t fs, const mk_instr &in,
+                      const SlotMeta &meta, uint32_t epoch, int cw, int lane) {
+  const uint32_t f = fs % kFifo, k = fs / kFifo;
+  if (cw == 0) {
+    int ok = 1;
+    if (lane == 0) {
+      ok = poll_counter(P, S, in, epoch, meta.idx);
+      if (ok) {
+        if (P.flags & MK_FLAG_TRACE) S.meta[f].t_ready = gtimer();
+        mbar_arrive(&S.rdy[f]);
+      }
+    }
+    if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+  }
+  return warp_wait(P, S, &S.rdy[f], k & 1u, kWhereCompute | meta.idx);
+}
+
+DEVI void finish_entry(const Smem &S, uint32_t fs, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.done[fs % kFifo]);
+}
+
+// Batch-1 run of consecutive GEMV instructions sharing the register input
+// cache; returns at the first attention or end entry (not consumed).
+DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t epoch, int cw,
+                      int lane) {
+  XCache X;
+  uint32_t xkey = 0xFFFFFFFFu;
+  while (true) {
+    const uint32_t f = fs % kFifo;
+    const mk_instr &in = S.fifo[f];
+    const SlotMeta &meta = S.meta[f];
+    if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return false;
+    if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, xkey))
+      return false;
+    finish_entry(S, fs, lane);
+    ++fs;
+    if (!next_entry(P, S, fs)) return false;
+    const uint8_t op = S.fifo[fs % kFifo].op;
+    if (op == MK_OP_ATTN || op == MK_OP_END) return true;
+  }
+}
+
+DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int lane) {
+  uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu;
+  uint32_t fs = 0;
+  if (!next_entry(P, S, fs)) return;
+  while (true) {
+    const uint32_t f = fs % kFifo;
+    const mk_instr &in = S.fifo[f];
+    const SlotMeta &meta = S.meta[f];
+    if (in.op == MK_OP_END) {
+      finish_entry(S, fs, lane);
+      return;
+    }
+    if (in.op != MK_OP_ATTN && P.B == 1) {
+      if (!run_gemv_b1(P, S, fs, epoch, cw, lane)) return;
+      continue;
+    }
+    if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return;
+    float *res = S.res + (size_t)f * P.res_floats;
+    bool ok;
+    if (in.op == MK_OP_ATTN) {
+      ok = attn_dispatch(P, S, in, meta, res, cw, lane, att_uses);
+      xkey = 0xFFFFFFFFu;
+    } else {
+      ok = gemv_bn(P, S, in, meta, res, cw, lane, xkey, xbar_uses, key_changes);
+    }
+    if (!ok) return;
+    finish_entry(S, fs, lane);
+    ++fs;
+    if (!next_entry(P, S, fs)) return;
+  }
+}
+
+// --------------------------------------------------------------- storer ----
+__device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
+                          const SlotMeta &meta, const float *res, int lane, uint32_t epoch) {
+  const int B = P.B, d = P.d;
+  const OpGeom &G = P.geom[in.op];
+  auto val = [&](uint32_t r, int b) {
+    float v = 0.f;
+    for (uint32_t s = 0; s < G.NS; ++s) v += res[(r * G.NS + s) * B + b];
+    return v;
+  };
+  uint32_t *ctr = P.ctr;
+  switch (in.op) {
+    case MK_OP_QKV: {
+      const int GR = (P.qpg + 2) * d;
+      const int grp = in.row0 / GR, q0 = in.row0 % GR;
+      const int half = d / 2;
+      if (q0 < (P.qpg + 1) * d) {  // q or k rows: rotate pairs
+        const bool is_q = q0 < P.qpg * d;
+        const int head_row0 = is_q ? q0 % d : q0 - P.qpg * d;
+        const int npairs = in.nrows / 2;
+        for (int u = lane; u < npairs * B; u += 32) {
+          const int pr = u % npairs, b = u / npairs;
+          const float x0 = val(2 * pr, b), x1 = val(2 * pr + 1, b);
+          const int i = (head_row0 + 2 * pr) / 2;
+          const float cs = S.rope[b * d + i], sn = S.rope[b * d + half + i];
+          const float o0 = x0 * cs - x1 * sn, o1 = x0 * sn + x1 * cs;
+          if (is_q) {
+            float *qd = P.q + ((size_t)b * P.nq + grp * P.qpg + q0 / d) * d;
+            qd[i] = o0;
+            qd[i + half] = o1;
+          } else {
+            uint16_t *kd = P.kc + kv_row(P, in.layer, b, grp, S.pos[b]);
+            kd[i] = to_bf(o0);
+            kd[i + half] = to_bf(o1);
+          }
+        }
+      } else {
+        const int dim0 = q0 - (P.qpg + 1) * d;
+        for (int u = lane; u < (int)in.nrows * B; u += 32) {
+          const int r = u % in.nrows, b = u / in.nrows;
+          P.vc[kv_row(P, in.layer, b, grp, S.pos[b]) + dim0 + r] = to_bf(val(r, b));
+        }
+      }
+      break;
+    }
+    case MK_OP_OPROJ:
+    case MK_OP_DOWN: {
+      for (int u = lane; u < (int)in.nrows * B; u += 32) {
+        const int r = u % in.nrows, b = u / in.nrows;
+        const int row = in.row0 + r;
+        float *xp = P.x + (size_t)b * P.H + row;
+        const float resid = (in.op == MK_OP_OPROJ && (in.flags & 1))
+                                ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
+                                : __ldcg(xp);
+        *xp = resid + val(r, b);
+      }
+      break;
+    }
+    case MK_OP_GATEUP: {
+      for (int u = lane; u < (int)in.nrows * B; u += 32) {
+        const int j = u % in.nrows, b = u / in.nrows;
+        const float gt = val(j, b), up = val(in.nrows + j, b);
+        P.h[(size_t)b * P.F + in.row0 + j] = gt / (1.f + __expf(-gt)) * up;
+      }
+      break;
+    }
+    case MK_OP_LMHEAD: {
+      for (int u = lane; u < (int)in.nrows * B; u += 32) {
+        const int r = u % in.nrows, b = u / in.nrows;
+        P.logits[(size_t)b * P.V + in.row0 + r] = val(r, b);
+      }
+      break;
+    }
+    case MK_OP_ATTN: {
+      const int qpg = P.qpg, PS = 2 * qpg + qpg * d;
+      float *dst = P.part + (((size_t)in.b * P.nkv + in.g) * P.nchunk + in.chunk) * PS;
+      for (int k = lane; k < PS; k += 32) dst[k] = res[k];
+      break;
+    }
+  }
+  fence_gpu();
+  __syncwarp();
+  if (in.op != MK_OP_ATTN) {
+    if (lane == 0) red_add(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+  } else {
+    uint32_t old = 0;
+    if (lane == 0) old = atom_add_acq_rel(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+    __syncwarp();
+    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+    if (old == epoch * in.nchunk + in.nchunk - 1u) {
+      // last chunk of (b, g): merge the chunk partials by log-sum-exp
+      const int qpg = P.qpg, PS = 2 * qpg + qpg * d, per = qpg * d / 32;
+      const float *pb = P.part + ((size_t)in.b * P.nkv + in.g) * P.nchunk * PS;
+      const int o0 = lane * per, h = o0 / d, dim0 = o0 % d;
+      float M = -INFINITY, den = 0.f, num[32];
+      for (int k = 0; k < per; ++k) num[k] = 0.f;
+      for (uint32_t c = 0; c < in.nchunk; ++c) {
+        const float *pc = pb + (size_t)c * PS;
+        const float mc = __ldcg(pc + h);
+        if (mc == -INFINITY) continue;
+        const float lc = __ldcg(pc + qpg + h);
+        const float Mn = fmaxf(M, mc);
+        const float a = __expf(M - Mn), w = __expf(mc - Mn);
+        den = den * a + w * lc;
+        for (int k = 0; k < per; ++k) num[k] = num[k] * a + w * __ldcg(pc + 2 * qpg + h * d + dim0 + k);
+        M = Mn;
+      }
+      float *out = P.attn + (size_t)in.b * P.nq * d + ((size_t)in.g * qpg + h) * d + dim0;
+      const float inv = 1.f / den;
+      for (int k = 0; k < per; ++k) out[k] = num[k] * inv;
+      fence_gpu();
+      __syncwarp();
+      if (lane == 0) red_add(ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
+    }
+  }
+  if (lane == 0) {
+    red_add(P.exec + meta.idx, 1u);
+    if (P.flags & MK_FLAG_TRACE) {
+      unsigned long long *tr = P.trace + (size_t)meta.idx * 4;
+      tr[0] = ((unsigned long long)smid() << 32) | blockIdx.x;
+      tr[1] = meta.t_claim;
+      tr[2] = meta.t_ready;
+      tr[3] = gtimer();
+    }
+  }
+}
+
+DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
+  for (uint32_t fs = 0;; ++fs) {
+    const uint32_t f = fs % kFifo, k = fs / kFifo;
+    if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
+    const mk_instr &in = S.fifo[f];
+    const SlotMeta &meta = S.meta[f];
+    if (in.op == MK_OP_END) break;
+    storer_epilogue(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.iempty[f]);
+  }
+}
+
+// --------------------------------------------------------------- kernel ----
+extern "C" __global__ void __launch_bounds__(kThreads, 1)
+    mk_megakernel(const __grid_constant__ KParams P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Smem S = make_smem(P, smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (uint32_t i = 0; i < P.ring_pages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kComputeWarps);
+    }
+    for (int i = 0; i < kFifo; ++i) {
+      mbar_init(&S.ifull[i], 1);
+      mbar_init(&S.iempty[i], 1);
+      mbar_init(&S.rdy[i], 1);
+      mbar_init(&S.done[i], kComputeWarps);
+    }
+    mbar_init(S.attbar, kComputeWarps);
+    mbar_init(S.xbar, kComputeWarps);
+    fence_mbar_init();
+    S.misc[0] = 0;
+    S.misc[1] = 0;
+  }
+  for (int i = tid; i < P.n_wait; i += kThreads) S.sat[i] = 0u;
+  const uint32_t epoch = ld_relaxed(P.ctrl + kCtlEpoch);
+  __syncthreads();
+  if (tid < P.B) {
+    const int t = P.tokens[tid], p = P.positions[tid];
+    S.tok[tid] = t;
+    S.pos[tid] = p;
+    if (t < 0 || t >= P.V || p < 0 || p >= P.max_ctx) S.misc[1] = 1;
+  }
+  __syncthreads();
+  const bool bad = S.misc[1] != 0;
+  if (!bad) {
+    const int half = P.d / 2;
+    for (int i = tid; i < P.B * half; i += kThreads) {
+      const int b = i / half, k = i % half;
+      const size_t at = (size_t)S.pos[b] * half + k;
+      S.rope[b * P.d + k] = P.rope_cos[at];
+      S.rope[b * P.d + half + k] = P.rope_sin[at];
+    }
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0 && blockIdx.x == 0) raise_error(P, MK_ERR_BOUNDS, 0, false);
+    return;
+  }
+  if (warp == 0) {
+    if (lane == 0) loader(P, S, epoch);
+    __syncwarp();
+  } else if (warp == 1) {
+    storer(P, S, epoch, lane);
+  } else {
+    compute(P, S, epoch, warp - 2, lane);
+  }
+  __syncthreads();
+  if (tid == 0 && P.mode != kModeRange && S.misc[0] == 0) {
+    fence_gpu();
+    const uint32_t old = atomicAdd(P.ctrl + kCtlExit, 1u);
+    if (old == epoch * P.n_blocks + P.n_blocks - 1u) atomicExch(P.ctrl + kCtlEpoch, epoch + 1u);
+  }
+}
+
+// The multi-kernel path ends each step with this one-thread launch.
+extern "C" __global__ void mk_epoch_advance(uint32_t *ctrl) { ctrl[kCtlEpoch] += 1u; }
+
+// Re-tiling of one weight block: tile-row k of a block whose source row is
+// map[k] (identity when map is NULL) is split into NS items of item_bytes,
+// packed ipp per page of `page` bytes; tiles are tile_stride bytes apart.
+extern "C" __global__ void mk_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                                     uint32_t nrows, uint32_t K, uint32_t NS,
+                                     uint32_t item_bytes, uint32_t ipp, uint32_t page,
+                                     uint32_t wrows_per_tile, uint64_t tile_stride) {
+  const uint64_t per_row = (uint64_t)K * 2 / 16;
+  const uint64_t total = (uint64_t)nrows * per_row;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = (uint32_t)(i / per_row);
+    const uint32_t cb = (uint32_t)(i % per_row) * 16;
+    const uint32_t s = cb / item_bytes, ib = cb % item_bytes;
+    const uint32_t t = k / wrows_per_tile, r = k % wrows_per_tile;
+    const uint32_t item = r * NS + s;
+    uint8_t *d = dst + t * tile_stride + (uint64_t)(item / ipp) * page +
+                 (uint64_t)(item % ipp) * item_bytes + ib;
+    const uint32_t srow = map ? (uint32_t)map[k] : k;
+    *reinterpret_cast<uint4 *>(d) =
+        *reinterpret_cast<const uint4 *>(src + (uint64_t)srow * K * 2 + cb);
+  }
+}
+
+// ---- host-side launch helpers (the kernels' host stubs live in this unit) ----
+cudaError_t set_megakernel_smem(uint32_t bytes) {
+  return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)bytes);
+}
+
+cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
+                              cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = P.smem_total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, mk_megakernel, P);
+}
+
+cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream) {
+  mk_epoch_advance<<<1, 1, 0, stream>>>(ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map, uint32_t nrows,
+                          const OpGeom &g, uint32_t page, uint64_t tile_stride,
+                          cudaStream_t stream) {
+  const uint64_t total = (uint64_t)nrows * g.K * 2 / 16;
+  const uint32_t blocks = (uint32_t)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
+  mk_retile<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, nrows, g.K, g.NS,
+                                                      g.item_bytes, g.ipp, page,
+                                                      g.wrows_per_tile, tile_stride);
+  return cudaGetLastError();
+}
+
+}  // namespace mk

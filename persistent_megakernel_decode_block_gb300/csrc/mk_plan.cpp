@@ -1,0 +1,360 @@
+// mk_plan.cpp -- the host planner.
+//
+// « 2 · Définition et généalogie », §2.5: the CPU builds the instruction
+// list; §2.6 gives the five mechanisms this table drives: persistence (one
+// block per SM), dispatch (one opcode per instruction), dependency counters
+// (one wait and one signal per instruction), the paged shared-memory
+// allocator (the ring and slot layout computed here) and scheduling (queue
+// order, or static per-SM lists).  The "one dependency event and one trigger
+// event per task" normal form and "tasks of one event at contiguous indices"
+// follow the MPK paragraph of the same chapter's questions: every
+// instruction has one wait counter and one signal counter, and the
+// instructions of one op and layer occupy one contiguous phase of the queue.
+#include "mk_plan.h"
+
+#include <string.h>
+
+#include <algorithm>
+
+namespace mk {
+
+static void geom_for(uint32_t K, uint32_t page, OpGeom &g) {
+  uint32_t NS = (K + 2047) / 2048;
+  while (K % (NS * 256)) NS++;
+  g.K = K;
+  g.NS = NS;
+  g.SW = K / NS;
+  g.item_bytes = 2 * g.SW;
+  g.ipp = page / g.item_bytes;
+  g.nch = g.SW / 256;
+}
+
+static uint32_t cdiv(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
+static uint64_t align_up(uint64_t a, uint64_t b) { return (a + b - 1) / b * b; }
+
+int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, HostPlan &P,
+               const char **why) {
+  static const char *ok = "ok";
+  *why = ok;
+  const mk_config &c = cfg;
+#define REJECT(msg)   \
+  do {                \
+    *why = msg;       \
+    return MK_ERR_CONFIG; \
+  } while (0)
+  if (c.n_layers < 1 || c.n_layers > 4096) REJECT("n_layers must be in 1..4096");
+  if (c.hidden < 256 || c.hidden % 256) REJECT("hidden must be a positive multiple of 256");
+  if (c.ffn_dim < 256 || c.ffn_dim % 256) REJECT("ffn_dim must be a positive multiple of 256");
+  if (c.n_kv_heads < 1 || c.n_q_heads < 1 || c.n_q_heads % c.n_kv_heads)
+    REJECT("n_q_heads must be a positive multiple of n_kv_heads");
+  if (c.n_q_heads / c.n_kv_heads > kMaxQpg) REJECT("at most 8 q heads per KV group");
+  if (c.head_dim != 64 && c.head_dim != 128) REJECT("head_dim must be 64 or 128");
+  if ((c.n_q_heads * c.head_dim) % 256) REJECT("n_q_heads*head_dim must be a multiple of 256");
+  if (c.vocab < 1) REJECT("vocab must be positive");
+  if (c.batch < 1 || c.batch > kMaxBatch) REJECT("batch must be in 1..16");
+  if (c.max_ctx < 16 || c.max_ctx % 16) REJECT("max_ctx must be a positive multiple of 16");
+  if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) REJECT("rms_eps >= 0 and rope_theta > 0 required");
+  if (c.sched_mode != MK_SCHED_DYNAMIC && c.sched_mode != MK_SCHED_STATIC) REJECT("bad sched_mode");
+  if (num_sms < 1 || num_sms > 1024) REJECT("number of SMs out of range");
+  const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : 16384u;
+  if (page < 4096 || page > 65536 || page % 1024) REJECT("page_bytes must be a multiple of 1024 in 4096..65536");
+
+  P = HostPlan();
+  P.cfg = c;
+  P.num_sms = num_sms;
+  P.smem_limit = smem_limit;
+  P.page_bytes = page;
+  const int L = c.n_layers, H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim,
+            F = c.ffn_dim, V = c.vocab, B = c.batch;
+  const int qpg = nq / nkv, GR = (qpg + 2) * d, QD = nq * d;
+
+  // ---- GEMV geometry and tile sizes ------------------------------------
+  geom_for(H, page, P.geom[MK_OP_QKV]);
+  geom_for(QD, page, P.geom[MK_OP_OPROJ]);
+  geom_for(H, page, P.geom[MK_OP_GATEUP]);
+  geom_for(F, page, P.geom[MK_OP_DOWN]);
+  geom_for(H, page, P.geom[MK_OP_LMHEAD]);
+  auto rows_for = [&](int op, uint64_t target_bytes, uint32_t wrows_per_out) {
+    OpGeom &g = P.geom[op];
+    uint32_t cap = kMaxItems / (g.NS * wrows_per_out);
+    uint64_t want = target_bytes / ((uint64_t)2 * g.K * wrows_per_out);
+    uint32_t r = (uint32_t)std::max<uint64_t>(1, std::min<uint64_t>(cap, want));
+    return std::max<uint32_t>(1, r);
+  };
+  {
+    uint32_t r = rows_for(MK_OP_QKV, 65536, 1);
+    r = std::max<uint32_t>(2, r - r % 2);
+    while (d % r) r -= 2;  // a tile never straddles a head; pairs stay whole
+    P.geom[MK_OP_QKV].rows_per_tile = r;
+    P.geom[MK_OP_QKV].wrows_per_tile = r;
+  }
+  P.geom[MK_OP_OPROJ].rows_per_tile = P.geom[MK_OP_OPROJ].wrows_per_tile = rows_for(MK_OP_OPROJ, 65536, 1);
+  P.geom[MK_OP_GATEUP].rows_per_tile = rows_for(MK_OP_GATEUP, 131072, 2);
+  P.geom[MK_OP_GATEUP].wrows_per_tile = 2 * P.geom[MK_OP_GATEUP].rows_per_tile;
+  P.geom[MK_OP_DOWN].rows_per_tile = P.geom[MK_OP_DOWN].wrows_per_tile = rows_for(MK_OP_DOWN, 131072, 1);
+  P.geom[MK_OP_LMHEAD].rows_per_tile = P.geom[MK_OP_LMHEAD].wrows_per_tile = rows_for(MK_OP_LMHEAD, 131072, 1);
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
+    if (op == MK_OP_ATTN) continue;
+    const OpGeom &g = P.geom[op];
+    if (g.ipp < 1 || g.nch > (uint32_t)kMaxChunks || g.NS > (uint32_t)kComputeWarps)
+      REJECT("GEMV geometry does not fit the compute warps");
+    if (g.wrows_per_tile * g.NS > (uint32_t)kMaxItems) REJECT("tile has too many items");
+  }
+  auto tile_pages = [&](int op, uint32_t wrows) { return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp); };
+
+  // ---- attention chunking ----------------------------------------------
+  uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : 0;
+  if (!ch) {
+    ch = 64;
+    while (ch < 256 && ch * 16 < (uint32_t)c.max_ctx) ch *= 2;
+  }
+  if (ch % 16 || ch < 16 || ch > 1024) REJECT("attn_chunk must be a multiple of 16 in 16..1024");
+  P.attn_chunk = ch;
+  P.nchunk = cdiv(c.max_ctx, ch);
+
+  // ---- counters ----------------------------------------------------------
+  P.n_wait = (uint32_t)L * (nkv + 4);
+  const uint32_t arr_base = P.n_wait;
+  P.lm_ctr = arr_base + (uint32_t)L * B * nkv;
+  P.n_ctr = P.lm_ctr + 1;
+  P.ctr_inc.assign(P.n_ctr, 0);
+
+  // ---- weight arena: norms, embedding, then tiles in queue order ---------
+  uint64_t off = 0;
+  P.off_norms = off;
+  off = align_up(off + (uint64_t)(2 * L + 1) * H * 2, 4096);
+  {
+    const OpGeom &g = P.geom[MK_OP_LMHEAD];
+    bool plain = (page % g.item_bytes == 0) && ((g.wrows_per_tile * g.NS) % g.ipp == 0);
+    P.embed_alias = c.tie_embeddings && plain;
+  }
+  if (!P.embed_alias) {
+    P.off_embed = off;
+    off = align_up(off + (uint64_t)V * H * 2, 4096);
+  }
+  off = align_up(off, page);
+
+  // ---- instructions --------------------------------------------------------
+  auto push = [&](mk_instr in) {
+    in.phase = (uint32_t)P.phases.size() - 1;
+    P.instr.push_back(in);
+    P.phases.back().count++;
+  };
+  auto new_phase = [&](uint32_t op, uint32_t layer) {
+    mk_phase ph{(uint32_t)P.instr.size(), 0, op, layer};
+    P.phases.push_back(ph);
+  };
+  auto base = [&](uint8_t op, int l) {
+    mk_instr in;
+    memset(&in, 0, sizeof in);
+    in.op = op;
+    in.layer = (uint16_t)l;
+    in.wait_ctr = MK_NO_COUNTER;
+    in.sig2_ctr = MK_NO_COUNTER;
+    return in;
+  };
+  const uint32_t nO = cdiv(H, P.geom[MK_OP_OPROJ].rows_per_tile);
+  const uint32_t nGU = cdiv(F, P.geom[MK_OP_GATEUP].rows_per_tile);
+  const uint32_t nD = cdiv(H, P.geom[MK_OP_DOWN].rows_per_tile);
+  const uint32_t nLM = cdiv(V, P.geom[MK_OP_LMHEAD].rows_per_tile);
+  const uint32_t qkv_r = P.geom[MK_OP_QKV].rows_per_tile, qkv_tiles_per_group = GR / qkv_r;
+  P.off_qkv.resize(L);
+  P.off_o.resize(L);
+  P.off_gu.resize(L);
+  P.off_d.resize(L);
+
+  auto gemv_tiles = [&](uint8_t op, int l, uint32_t nout, uint32_t ntiles, mk_instr proto) {
+    const OpGeom &g = P.geom[op];
+    const uint32_t full_pages = tile_pages(op, g.wrows_per_tile);
+    for (uint32_t t = 0; t < ntiles; ++t) {
+      mk_instr in = proto;
+      in.row0 = t * g.rows_per_tile;
+      in.nrows = std::min<uint32_t>(g.rows_per_tile, nout - in.row0);
+      uint32_t wrows = op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+      in.npages = tile_pages(op, wrows);
+      in.wofs = off + (uint64_t)t * full_pages * page;
+      P.weight_bytes += (uint64_t)wrows * g.K * 2;
+      push(in);
+      P.ctr_inc[in.sig_ctr]++;
+    }
+    off += (uint64_t)(ntiles - 1) * full_pages * page +
+           (uint64_t)tile_pages(op, op == MK_OP_GATEUP
+                                        ? 2 * (nout - (ntiles - 1) * g.rows_per_tile)
+                                        : nout - (ntiles - 1) * g.rows_per_tile) * page;
+    off = align_up(off, page);
+  };
+
+  for (int l = 0; l < L; ++l) {
+    // RMSNorm + QKV + RoPE, group-major so a group's attention can start early
+    new_phase(MK_OP_QKV, l);
+    P.off_qkv[l] = off;
+    {
+      const OpGeom &g = P.geom[MK_OP_QKV];
+      const uint32_t tp = tile_pages(MK_OP_QKV, qkv_r);
+      for (int grp = 0; grp < nkv; ++grp)
+        for (uint32_t t = 0; t < qkv_tiles_per_group; ++t) {
+          mk_instr in = base(MK_OP_QKV, l);
+          in.flags = l == 0 ? 1 : 0;
+          in.g = (uint16_t)grp;
+          if (l > 0) {
+            in.wait_ctr = ctr_d(c, l - 1);
+            in.wait_tgt = nD;
+          }
+          in.sig_ctr = ctr_qkv(c, l, grp);
+          in.row0 = grp * GR + t * qkv_r;
+          in.nrows = qkv_r;
+          in.npages = tp;
+          in.wofs = off;
+          off += (uint64_t)tp * page;
+          P.weight_bytes += (uint64_t)qkv_r * g.K * 2;
+          push(in);
+          P.ctr_inc[in.sig_ctr]++;
+        }
+    }
+    // attention chunks, group-major
+    new_phase(MK_OP_ATTN, l);
+    for (int grp = 0; grp < nkv; ++grp)
+      for (int b = 0; b < B; ++b)
+        for (uint32_t ck = 0; ck < P.nchunk; ++ck) {
+          mk_instr in = base(MK_OP_ATTN, l);
+          in.b = (uint16_t)b;
+          in.g = (uint16_t)grp;
+          in.wait_ctr = ctr_qkv(c, l, grp);
+          in.wait_tgt = qkv_tiles_per_group;
+          in.sig_ctr = arr_base + ((uint32_t)l * B + b) * nkv + grp;
+          in.sig2_ctr = ctr_attn(c, l);
+          in.sig2_after = P.nchunk;
+          in.chunk = ck;
+          in.nchunk = P.nchunk;
+          push(in);
+          P.ctr_inc[in.sig_ctr]++;
+          if (ck == 0) P.ctr_inc[in.sig2_ctr]++;
+        }
+    // O-projection + residual
+    new_phase(MK_OP_OPROJ, l);
+    P.off_o[l] = off;
+    {
+      mk_instr in = base(MK_OP_OPROJ, l);
+      in.flags = l == 0 ? 1 : 0;
+      in.wait_ctr = ctr_attn(c, l);
+      in.wait_tgt = (uint32_t)B * nkv;
+      in.sig_ctr = ctr_o(c, l);
+      gemv_tiles(MK_OP_OPROJ, l, H, nO, in);
+    }
+    // RMSNorm + gate/up + SiLU*mul
+    new_phase(MK_OP_GATEUP, l);
+    P.off_gu[l] = off;
+    {
+      mk_instr in = base(MK_OP_GATEUP, l);
+      in.wait_ctr = ctr_o(c, l);
+      in.wait_tgt = nO;
+      in.sig_ctr = ctr_gu(c, l);
+      gemv_tiles(MK_OP_GATEUP, l, F, nGU, in);
+    }
+    // down-projection + residual
+    new_phase(MK_OP_DOWN, l);
+    P.off_d[l] = off;
+    {
+      mk_instr in = base(MK_OP_DOWN, l);
+      in.wait_ctr = ctr_gu(c, l);
+      in.wait_tgt = nGU;
+      in.sig_ctr = ctr_d(c, l);
+      gemv_tiles(MK_OP_DOWN, l, H, nD, in);
+    }
+  }
+  new_phase(MK_OP_LMHEAD, 0);
+  P.off_lm = off;
+  {
+    mk_instr in = base(MK_OP_LMHEAD, 0);
+    in.wait_ctr = ctr_d(c, L - 1);
+    in.wait_tgt = nD;
+    in.sig_ctr = P.lm_ctr;
+    gemv_tiles(MK_OP_LMHEAD, 0, V, nLM, in);
+  }
+  P.arena_bytes = align_up(off, 4096);
+
+  // test-only fault: one wait target that can never be reached
+  if (c.flags & MK_FLAG_FAULT_WAIT) {
+    const mk_phase &ph = P.phases[5 * (L - 1) + 2];  // O-projection of the last layer
+    P.fault_instr = ph.first;
+    P.instr[ph.first].wait_tgt += 1;
+  }
+
+  // ---- static per-SM lists: round-robin over the queue order -------------
+  P.list_off.assign(num_sms + 1, 0);
+  for (uint32_t s = 0; s < num_sms; ++s)
+    P.list_off[s + 1] = P.list_off[s] + (uint32_t)((P.instr.size() + num_sms - 1 - s) / num_sms);
+  P.list_idx.resize(P.instr.size());
+  for (uint32_t s = 0, k = 0; s < num_sms; ++s)
+    for (size_t i = s; i < P.instr.size(); i += num_sms) P.list_idx[k++] = (uint32_t)i;
+
+  // ---- re-tiling maps ----------------------------------------------------
+  P.qkv_map.resize((size_t)(nq + 2 * nkv) * d);
+  for (int R = 0; R < (nq + 2 * nkv) * d; ++R) {
+    int grp = R / GR, q = R % GR;
+    auto pair_to_natural = [&](int ip) { return ip % 2 == 0 ? ip / 2 : ip / 2 + d / 2; };
+    int nat;
+    if (q < qpg * d)
+      nat = (grp * qpg + q / d) * d + pair_to_natural(q % d);
+    else if (q < (qpg + 1) * d)
+      nat = QD + grp * d + pair_to_natural(q - qpg * d);
+    else
+      nat = QD + nkv * d + grp * d + (q - (qpg + 1) * d);
+    P.qkv_map[R] = nat;
+  }
+  {
+    const uint32_t r = P.geom[MK_OP_GATEUP].rows_per_tile;
+    P.gu_map.resize((size_t)2 * F);
+    size_t k = 0;
+    for (uint32_t t = 0; t < nGU; ++t) {
+      uint32_t r0 = t * r, nr = std::min<uint32_t>(r, F - r0);
+      for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(r0 + j);
+      for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(F + r0 + j);
+    }
+  }
+
+  // ---- shared-memory layout -------------------------------------------------
+  P.res_floats = (uint32_t)std::max(kMaxItems * B, 2 * qpg + qpg * d);
+  P.res_floats = (P.res_floats + 3) / 4 * 4;
+  uint32_t fixed = 0;
+  auto take = [&](uint32_t bytes, uint32_t align) {
+    fixed = (uint32_t)align_up(fixed, align);
+    uint32_t at = fixed;
+    fixed += bytes;
+    return at;
+  };
+  // offsets are relative to the end of the ring; rebased below
+  uint32_t rel_fifo = take(kFifo * 64, 64);
+  uint32_t rel_meta = take(kFifo * sizeof(SlotMeta), 16);
+  uint32_t rel_res = take(kFifo * P.res_floats * 4, 16);
+  uint32_t att_bytes = (qpg * ch + kComputeWarps * d + kComputeWarps) * 4;
+  uint32_t rel_att = take(att_bytes, 16);
+  uint32_t rel_sat = take(P.n_wait * 4, 16);
+  uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
+  uint32_t rel_rope = take(B * d * 4, 16);
+  uint32_t rel_normr = take(kMaxBatch * 4, 16);
+  uint32_t rel_misc = take(64, 16);
+  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 2) * 8;
+  uint32_t rel_bars = take(bars_max, 8);
+  uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
+  uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);
+  if (E < 2) REJECT("shared memory too small for a two-page ring");
+  P.ring_pages = E;
+  uint32_t ring = (uint32_t)align_up(E * page, 1024);
+  P.off_fifo = ring + rel_fifo;
+  P.off_meta = ring + rel_meta;
+  P.off_res = ring + rel_res;
+  P.off_att = ring + rel_att;
+  P.off_sat = ring + rel_sat;
+  P.off_pos = ring + rel_pos;
+  P.off_rope = ring + rel_rope;
+  P.off_normr = ring + rel_normr;
+  P.off_misc = ring + rel_misc;
+  P.off_bars = ring + rel_bars;
+  P.smem_total = ring + fixed;
+  if (P.smem_total > smem_limit) REJECT("shared-memory layout exceeds the limit");
+#undef REJECT
+  return MK_OK;
+}
+
+}  // namespace mk

@@ -1,0 +1,167 @@
+"""CPU tests of the C ABI: the library loads and exports every symbol that
+include/mk.h declares; host-only planning of every workload replays cleanly
+against the oracle's independent replay (bit-exact counter increments,
+hazards, coverage, deadlock search); tables are deterministic; host-side
+errors come back as codes with nothing launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from persistent_megakernel_decode_block_gb300 import mk
+from synth.workloads import ORDER, WORKLOADS, max_ctx
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mk.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MK_API\s+[\w\s\*]+?\b(mk_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 17
+    L = ctypes.CDLL(mk.LIB)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def host_plan(name, n_sms=152, **kw):
+    w = WORKLOADS[name]
+    cfg = mk.make_config(w["model"], w["batch"], max_ctx(name), num_sms=n_sms,
+                         flags=mk.MK_FLAG_HOST_ONLY | kw.pop("flags", 0), **kw)
+    return mk.mk_plan(cfg)
+
+
+@pytest.mark.parametrize("name", ORDER)
+def test_plan_replays_against_the_oracle(name):
+    w = WORKLOADS[name]
+    p = host_plan(name)
+    try:
+        info = mk.mk_plan_info(p)
+        rec, raw, inc = mk.mk_plan_tables(p)
+        off, idx = mk.mk_plan_lists(p)
+        want = oracle.replay(raw, info["n_instr"], info["n_counters"], w["model"], w["batch"],
+                             info["n_blocks"], off, idx)
+        assert np.array_equal(inc, want)
+        # weights are streamed exactly once per step
+        m = w["model"]
+        H, F, V, L = m["hidden"], m["ffn_dim"], m["vocab"], m["n_layers"]
+        QD, KD = m["n_q_heads"] * m["head_dim"], m["n_kv_heads"] * m["head_dim"]
+        per_layer = (QD + 2 * KD) * H + H * QD + 2 * F * H + H * F
+        assert info["weight_bytes"] == 2 * (L * per_layer + V * H)
+        # the phase table partitions the queue
+        ph = mk.mk_plan_phases(p)
+        assert sum(c for _, c, _, _ in ph) == info["n_instr"]
+        assert all(rec["phase"][f:f + c].tolist() == [i] * c for i, (f, c, _, _) in enumerate(ph))
+    finally:
+        mk.mk_destroy(p)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama1b_ctx1024", "llama1b_b8_ragged"])
+@pytest.mark.parametrize("mode", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC])
+def test_plan_never_deadlocks_in_simulation(name, mode):
+    p = host_plan(name, n_sms=40, sched_mode=mode)
+    try:
+        info = mk.mk_plan_info(p)
+        _, raw, _ = mk.mk_plan_tables(p)
+        lists = mk.mk_plan_lists(p) if mode == mk.MK_SCHED_STATIC else (None, None)
+        oracle.simulate(raw, info["n_instr"], info["n_counters"], info["n_blocks"],
+                        info["fifo_depth"], seed=11, trials=3, list_off=lists[0],
+                        list_idx=lists[1])
+    finally:
+        mk.mk_destroy(p)
+
+
+def test_tiny_plan_exhaustive_two_sm_search():
+    # every interleaving of two SMs with FIFO depth 1 finishes (tiny plan)
+    w = WORKLOADS["tiny"]
+    cfg = mk.make_config(w["model"], 1, 128, num_sms=2, flags=mk.MK_FLAG_HOST_ONLY)
+    p = mk.mk_plan(cfg)
+    try:
+        info = mk.mk_plan_info(p)
+        _, raw, _ = mk.mk_plan_tables(p)
+        assert oracle.explore(raw, info["n_instr"], info["n_counters"], 1) > info["n_instr"]
+    finally:
+        mk.mk_destroy(p)
+
+
+def test_tables_are_deterministic():
+    a, b = host_plan("llama1b_b8_ragged"), host_plan("llama1b_b8_ragged")
+    try:
+        assert np.array_equal(mk.mk_plan_tables(a)[1], mk.mk_plan_tables(b)[1])
+        assert np.array_equal(mk.mk_plan_tables(a)[2], mk.mk_plan_tables(b)[2])
+    finally:
+        mk.mk_destroy(a)
+        mk.mk_destroy(b)
+
+
+def test_fault_flag_makes_one_target_unreachable():
+    w = WORKLOADS["tiny"]
+    p = host_plan("tiny", flags=mk.MK_FLAG_FAULT_WAIT)
+    try:
+        info = mk.mk_plan_info(p)
+        _, raw, _ = mk.mk_plan_tables(p)
+        with pytest.raises(AssertionError, match="signals per step|waits for"):
+            oracle.replay(raw, info["n_instr"], info["n_counters"], w["model"], 1,
+                          info["n_blocks"])
+    finally:
+        mk.mk_destroy(p)
+
+
+@pytest.mark.parametrize("field, value", [
+    ("hidden", 200), ("ffn_dim", 300), ("n_q_heads", 6), ("head_dim", 96), ("batch", 0),
+    ("batch", 17), ("max_ctx", 100), ("page_bytes", 1000), ("n_layers", 0), ("attn_chunk", 24),
+])
+def test_invalid_configs_are_rejected(field, value):
+    w = WORKLOADS["tiny"]
+    cfg = mk.make_config(w["model"], 1, 128, num_sms=8, flags=mk.MK_FLAG_HOST_ONLY)
+    setattr(cfg, field, value)
+    with pytest.raises(mk.MkError) as e:
+        mk.mk_plan(cfg)
+    assert e.value.code == mk.MK_ERR_CONFIG
+
+
+def test_host_only_plan_refuses_device_calls():
+    p = host_plan("tiny")
+    try:
+        buf = np.zeros(4, np.int32)
+        with pytest.raises(mk.MkError) as e:
+            mk.mk_decode_step(p, buf, buf, (buf, buf), buf)
+        assert e.value.code == mk.MK_ERR_STATE
+        with pytest.raises(mk.MkError) as e:
+            mk.mk_decode_step(p, None, buf, (buf, buf), buf)
+        assert e.value.code == mk.MK_ERR_ARG
+        assert mk.mk_status(p) == mk.MK_ERR_STATE
+    finally:
+        mk.mk_destroy(p)
+
+
+def test_error_strings():
+    for code in [0] + list(mk.ERRORS):
+        assert mk.mk_error_string(code)
+    assert mk.mk_error_string(12345) == "unknown error"
+
+
+def test_record_layout_matches_header():
+    # offsets documented in mk.h and restated in the oracle's replay
+    names = [n for n in mk.INSTR_DTYPE.names]
+    offs = [mk.INSTR_DTYPE.fields[n][1] for n in names]
+    assert dict(zip(names, offs)) == {
+        "op": 0, "flags": 1, "layer": 2, "b": 4, "g": 6, "wait_ctr": 8, "wait_tgt": 12,
+        "sig_ctr": 16, "sig2_ctr": 20, "sig2_after": 24, "row0": 28, "nrows": 32, "chunk": 36,
+        "nchunk": 40, "npages": 44, "wofs": 48, "phase": 56, "reserved": 60}
+
+
+def test_without_a_gpu_planning_on_the_device_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    w = WORKLOADS["tiny"]
+    with pytest.raises(mk.MkError) as e:
+        mk.mk_plan(mk.make_config(w["model"], 1, 128))
+    assert e.value.code == mk.MK_ERR_DEVICE
