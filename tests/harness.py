@@ -22,7 +22,7 @@ class Setup:
     def __init__(self, name, seed=0, steps=None, sched=mk.MK_SCHED_DYNAMIC, flags=0, tie=None,
                  with_oracle=True, timeout_us=0, **plan_kw):
         w = WORKLOADS[name]
-        self.name, self.seed = name, seed
+        self.name, self.seed, self.sched = name, seed, sched
         self.m = dict(w["model"])
         if tie is not None:
             self.m["tie_embeddings"] = int(tie)
@@ -74,7 +74,10 @@ class Setup:
                             self.info["n_blocks"])
         e = n_mega + n_multi
         ctr = (inc.astype(np.uint64) * e % 2 ** 32).astype(np.uint32)
-        queue = (n_mega * (self.info["n_instr"] + self.info["n_blocks"])) % 2 ** 32
+        # the work queue is only claimed in dynamic mode: N claims plus one
+        # past-the-end claim per block and step
+        queue = 0 if self.sched == mk.MK_SCHED_STATIC else (
+            n_mega * (self.info["n_instr"] + self.info["n_blocks"])) % 2 ** 32
         return ctr, queue, np.full(self.info["n_instr"], e, np.uint32), e
 
 
