@@ -1042,6 +1042,8 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     compute(P, S, epoch, warp - 2, lane);
   }
   __syncthreads();
+  // a block only bails after a latched error; never let it end silently
+  if (tid == 0 && S.misc[0] != 0) raise_error(P, MK_ERR_TIMEOUT, 0x0FFFFFFFu, true);
   if (tid == 0 && P.mode != kModeRange && S.misc[0] == 0) {
     fence_gpu();
     const uint32_t old = atomicAdd(P.ctrl + kCtlExit, 1u);

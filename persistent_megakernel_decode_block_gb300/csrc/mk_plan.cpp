@@ -332,7 +332,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_sat = take(P.n_wait * 4, 16);
   uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
   uint32_t rel_rope = take(B * d * 4, 16);
-  uint32_t rel_normr = take(kMaxBatch * 4, 16);
+  uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
   uint32_t rel_misc = take(64, 16);
   uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 2) * 8;
   uint32_t rel_bars = take(bars_max, 8);
