@@ -268,8 +268,9 @@ MK_API int mk_status(mk_plan_t plan, void *stream);
 MK_API int mk_read_counters(mk_plan_t plan, uint32_t *counters, uint32_t *queue, uint32_t *exec,
                             uint32_t *epoch);
 
-/* With MK_FLAG_TRACE: n_instr records of 4 u64 {sm id << 32 | block,
-   t_claim, t_ready, t_done} (%globaltimer ns) of the last step. */
+/* With MK_FLAG_TRACE: n_instr records of 8 u64 {sm id << 32 | block,
+   t_published, t_ready, t_done, t_pages_issued, t_compute_done,
+   t_storer_start, 0} (%globaltimer ns) of the last step. */
 MK_API int mk_read_trace(mk_plan_t plan, uint64_t *trace);
 
 MK_API int mk_debug_buffers(mk_plan_t plan, mk_debug_buffers_t *out);

@@ -66,8 +66,11 @@ struct KParams {
 // per FIFO slot metadata written by the loader
 struct SlotMeta {
   uint32_t idx, seq0, npages, pad;
-  unsigned long long t_claim, t_ready;
+  // trace timestamps (%globaltimer, MK_FLAG_TRACE only): published by the
+  // loader, last page issued, input ready, compute done, storer start
+  unsigned long long t_claim, t_issued, t_ready, t_cdone, t_sstart, pad2;
 };
+constexpr int kTraceWords = 8;  // u64 per instruction in the trace buffer
 
 #ifdef __CUDACC__
 cudaError_t set_megakernel_smem(uint32_t bytes);

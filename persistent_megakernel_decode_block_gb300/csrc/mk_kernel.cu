@@ -332,6 +332,7 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
       bulk_g2s(S.ring + (size_t)slot * PG, gsrc, bytes, &S.full[slot], pol);
       ++seq;
     }
+    if (P.flags & MK_FLAG_TRACE) m.t_issued = gtimer();
   }
   if (!ok) drain_copies(P, S, seq);
 }
@@ -787,9 +788,12 @@ DEVI bool ready_entry(const KParams &P, const Smem &S, uint32_t fs, const mk_ins
   return warp_wait(P, S, &S.rdy[f], k & 1u, kWhereCompute | meta.idx);
 }
 
-DEVI void finish_entry(const Smem &S, uint32_t fs, int lane) {
+DEVI void finish_entry(const KParams &P, const Smem &S, uint32_t fs, int cw, int lane) {
   __syncwarp();
-  if (lane == 0) mbar_arrive(&S.done[fs % kFifo]);
+  if (lane == 0) {
+    if (cw == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[fs % kFifo].t_cdone = gtimer();
+    mbar_arrive(&S.done[fs % kFifo]);
+  }
 }
 
 // Batch-1 run of consecutive GEMV instructions sharing the register input
@@ -805,7 +809,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return false;
     if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, xkey))
       return false;
-    finish_entry(S, fs, lane);
+    finish_entry(P, S, fs, cw, lane);
     ++fs;
     if (!next_entry(P, S, fs)) return false;
     const uint8_t op = S.fifo[fs % kFifo].op;
@@ -822,7 +826,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
     const mk_instr &in = S.fifo[f];
     const SlotMeta &meta = S.meta[f];
     if (in.op == MK_OP_END) {
-      finish_entry(S, fs, lane);
+      finish_entry(P, S, fs, cw, lane);
       return;
     }
     if (in.op != MK_OP_ATTN && P.B == 1) {
@@ -839,7 +843,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       ok = gemv_bn(P, S, in, meta, res, cw, lane, xkey, xbar_uses, key_changes);
     }
     if (!ok) return;
-    finish_entry(S, fs, lane);
+    finish_entry(P, S, fs, cw, lane);
     ++fs;
     if (!next_entry(P, S, fs)) return;
   }
@@ -963,11 +967,15 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
   if (lane == 0) {
     red_add(P.exec + meta.idx, 1u);
     if (P.flags & MK_FLAG_TRACE) {
-      unsigned long long *tr = P.trace + (size_t)meta.idx * 4;
+      unsigned long long *tr = P.trace + (size_t)meta.idx * kTraceWords;
       tr[0] = ((unsigned long long)smid() << 32) | blockIdx.x;
       tr[1] = meta.t_claim;
       tr[2] = meta.t_ready;
       tr[3] = gtimer();
+      tr[4] = meta.t_issued;
+      tr[5] = meta.t_cdone;
+      tr[6] = meta.t_sstart;
+      tr[7] = 0;
     }
   }
 }
@@ -979,6 +987,8 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
     const mk_instr &in = S.fifo[f];
     const SlotMeta &meta = S.meta[f];
     if (in.op == MK_OP_END) break;
+    if (lane == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[f].t_sstart = gtimer();
+    __syncwarp();
     storer_epilogue(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.iempty[f]);

@@ -116,7 +116,7 @@ static int setup_device(mk_plan_s *p) {
   AL(p->d_ctrl, (size_t)kCtlWords);
   AL(p->d_exec, N);
   AL(p->d_ctr_inc, (size_t)H.n_ctr);
-  if (c.flags & MK_FLAG_TRACE) AL(p->d_trace, N * 4);
+  if (c.flags & MK_FLAG_TRACE) AL(p->d_trace, N * kTraceWords);
   AL(p->d_x, (size_t)B * c.hidden);
   AL(p->d_q, (size_t)B * c.n_q_heads * d);
   AL(p->d_attn, (size_t)B * c.n_q_heads * d);
@@ -573,7 +573,7 @@ MK_API int mk_read_trace(mk_plan_t p, uint64_t *trace) {
   if (p->host_only || !p->d_trace) return MK_ERR_STATE;
   cudaSetDevice(p->device);
   CK(cudaDeviceSynchronize());
-  CK(cudaMemcpy(trace, p->d_trace, p->H.instr.size() * 32, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(trace, p->d_trace, p->H.instr.size() * kTraceWords * 8, cudaMemcpyDeviceToHost));
   return MK_OK;
 }
 
