@@ -281,6 +281,35 @@ MK_API int mk_reset(mk_plan_t plan, void *stream);
 /* Free everything the plan owns (synchronises the device first). NULL is a no-op. */
 MK_API void mk_destroy(mk_plan_t plan);
 
+/* Grouped-query decode attention that allocates no device memory (the pages
+   have no counterpart: this exists for callers that cannot allocate, e.g. a
+   serving engine whose device memory is all owned and budgeted by its own
+   allocator, or a latency-critical decode loop that must not pay for a
+   cudaMalloc).  It needs no plan.  For every sequence b and KV group g it
+   computes, for the q heads of that group, softmax(q . k_j / sqrt(d)) . v_j
+   over positions j = 0..positions[b] -- the megakernel's attention step,
+   split over KV chunks and merged by log-sum-exp.
+     q          device fp32 [B][n_q_heads][d]   (already rotated)
+     k_cache    device bf16 [B][n_kv_heads][max_ctx][d]  (one layer of the
+     v_cache    cache layout of mk_kv_cache, i.e. k + l*B*nkv*max_ctx*d)
+     positions  device int32 [B]; an out-of-range position yields NaN rows
+     out        device fp32 [B][n_q_heads * d]
+   The chunk partials live in one fixed 4 MiB static device array of the
+   library (1,048,576 floats; every GPU that loads the library holds it
+   until exit); B * n_kv_heads * nchunk * (2*qpg + qpg*d) floats must fit,
+   where nchunk = ceil(max_ctx / chunk), chunk = the power of two in 64..256
+   nearest above max_ctx/16, else MK_ERR_ARG (nothing launched).  The first
+   call on a device resolves the array's device address (once per device,
+   with that device current); make that first call before any stream
+   capture.  All calls share the array: calls that overlap on the GPU race.
+   Asynchronous on `stream`; calls no allocating routine.  Errors: MK_ERR_ARG
+   (NULL pointer, unsupported shape, too large for the scratch),
+   MK_ERR_DEVICE, MK_ERR_CUDA, MK_ERR_LAUNCH. */
+MK_API int mk_attention_noalloc(const float *q, const void *k_cache, const void *v_cache,
+                                const int32_t *positions, float *out, int32_t batch,
+                                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                int32_t max_ctx, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

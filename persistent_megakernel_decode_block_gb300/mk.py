@@ -286,3 +286,14 @@ def mk_reset(plan, stream=None):
 
 def mk_destroy(plan):
     lib().mk_destroy(plan)
+
+
+def mk_attention_noalloc(q, k_cache, v_cache, positions, out, batch, n_q_heads, n_kv_heads,
+                         head_dim, max_ctx, stream=None):
+    """Decode attention for callers that cannot allocate device memory: its
+    scratch is the library's fixed static device array (see mk.h)."""
+    f = lib().mk_attention_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [_vp] * 5 + [_i32] * 5 + [_vp]
+    _check(f(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions), _ptr(out), batch,
+             n_q_heads, n_kv_heads, head_dim, max_ctx, _stream(stream)), "mk_attention_noalloc")
