@@ -87,7 +87,7 @@ typedef struct mk_config {
   int32_t wait_timeout_us; /* device-side wait limit; 0 -> 1,000,000 */
   int32_t num_sms;         /* 0 -> query the device; >0 overrides (host-only planning) */
   int32_t smem_bytes;      /* 0 -> device opt-in maximum per block */
-  int32_t page_bytes;      /* shared-memory page size; 0 -> 16384 */
+  int32_t page_bytes;      /* shared-memory page size; 0 -> 32768 */
   int32_t attn_chunk;      /* max KV positions per attention instruction; 0 -> auto */
 } mk_config;
 
@@ -268,9 +268,11 @@ MK_API int mk_status(mk_plan_t plan, void *stream);
 MK_API int mk_read_counters(mk_plan_t plan, uint32_t *counters, uint32_t *queue, uint32_t *exec,
                             uint32_t *epoch);
 
-/* With MK_FLAG_TRACE: n_instr records of 8 u64 {sm id << 32 | block,
+/* With MK_FLAG_TRACE: n_instr records of 10 u64 {sm id << 32 | block,
    t_published, t_ready, t_done, t_pages_issued, t_compute_done,
-   t_storer_start, 0} (%globaltimer ns) of the last step. */
+   t_storer_start, t_input_loaded, t_first_page, t_last_page}
+   (%globaltimer ns) of the last step; the last three are recorded for
+   batch-1 GEMV instructions only. */
 MK_API int mk_read_trace(mk_plan_t plan, uint64_t *trace);
 
 MK_API int mk_debug_buffers(mk_plan_t plan, mk_debug_buffers_t *out);

@@ -12,7 +12,7 @@ namespace mk {
 // storer; the scheduler role is the loader's queue claim).
 constexpr int kComputeWarps = 14;  // 16 warps per block: 4 per SM sub-partition, 128 registers each
 constexpr int kThreads = 32 * (2 + kComputeWarps);
-constexpr int kFifo = 8;        // instructions a block may hold ahead of compute
+constexpr int kFifo = 12;       // instructions a block may hold ahead of compute
 constexpr int kMaxBatch = 16;
 constexpr int kMaxQpg = 8;      // q heads per KV group
 constexpr int kMaxItems = 32;   // work items (row x slice) per GEMV instruction
@@ -57,10 +57,11 @@ struct KParams {
   int32_t n_wait, mode;
   uint32_t range_first, range_count, n_blocks, flags;
   uint64_t timeout_ns;
+  uint32_t lookahead;  // FIFO entries the loader may publish ahead of its stream
   // dynamic shared-memory layout (byte offsets)
   uint32_t ring_pages, page_bytes;
   uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,
-      off_rope, off_normr, off_misc, smem_total;
+      off_rope, off_normr, off_misc, off_rbuf, off_xs, smem_total;
 };
 
 // per FIFO slot metadata written by the loader
@@ -68,9 +69,9 @@ struct SlotMeta {
   uint32_t idx, seq0, npages, pad;
   // trace timestamps (%globaltimer, MK_FLAG_TRACE only): published by the
   // loader, last page issued, input ready, compute done, storer start
-  unsigned long long t_claim, t_issued, t_ready, t_cdone, t_sstart, pad2;
+  unsigned long long t_claim, t_issued, t_ready, t_cdone, t_sstart, t_input, t_page0, t_pagel;
 };
-constexpr int kTraceWords = 8;  // u64 per instruction in the trace buffer
+constexpr int kTraceWords = 10;  // u64 per instruction in the trace buffer
 
 #ifdef __CUDACC__
 cudaError_t set_megakernel_smem(uint32_t bytes);

@@ -57,6 +57,18 @@ DEVI bool mbar_try_wait(uint64_t *b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// non-blocking test of a phase
+DEVI bool mbar_test(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 DEVI uint64_t policy_evict_first() {
   uint64_t p;
@@ -121,7 +133,7 @@ struct Smem {
   uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar;
   mk_instr *fifo;
   SlotMeta *meta;
-  float *res, *att_s, *opart, *lpart, *rope, *normr;
+  float *res, *att_s, *opart, *lpart, *rope, *normr, *rbuf, *xs;
   uint32_t *sat;
   int32_t *pos, *tok;
   volatile int *misc;  // [0] bail, [1] bad input
@@ -152,6 +164,8 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.rope = reinterpret_cast<float *>(base + P.off_rope);
   S.normr = reinterpret_cast<float *>(base + P.off_normr);
   S.misc = reinterpret_cast<volatile int *>(base + P.off_misc);
+  S.rbuf = reinterpret_cast<float *>(base + P.off_rbuf);
+  S.xs = reinterpret_cast<float *>(base + P.off_xs);
   return S;
 }
 
@@ -274,6 +288,24 @@ DEVI void drain_copies(const KParams &P, const Smem &S, uint32_t seq) {
   }
 }
 
+// The loader is one thread running two cursors over the FIFO:
+//  * claim cursor: takes the next instruction (queue claim, list entry or
+//    range), copies its record into a free FIFO slot with its page range and
+//    publishes it -- up to P.lookahead entries ahead of the stream cursor,
+//    independently of any dependency.  Claims and record loads are issued two
+//    instructions ahead so a burst of publishes does not wait on them;
+//  * stream cursor: copies the published pages, in order, into the
+//    shared-memory ring as slots are released by the compute warps.
+// Nothing here waits on a dependency counter, so the weights of later
+// instructions keep flowing while the compute warps wait (pages' §5.4).
+DEVI void load_record(const KParams &P, uint32_t idx, uint4 (&r)[4]) {
+  if (idx < P.n_instr) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(P.instr + idx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __ldg(src + i);
+  }
+}
+
 DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   const uint64_t pol = policy_evict_first();
   const uint32_t N = P.n_instr, E = P.ring_pages, PG = P.page_bytes;
@@ -283,58 +315,102 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
     list_k = P.list_off[blockIdx.x];
     list_end = P.list_off[blockIdx.x + 1];
   }
+  // every block takes exactly one past-the-end claim: no claim follows an
+  // index >= N
   auto claim = [&]() -> uint32_t {
     if (P.mode == kModeDynamic) return atomicAdd(P.ctrl + kCtlQueue, 1u) - qbase;
-    if (P.mode == kModeStatic) return list_k < list_end ? P.list_idx[list_k++] : N;
+    if (P.mode == kModeStatic) return list_k < list_end ? __ldg(P.list_idx + list_k++) : N;
     const uint32_t r = range_taken ? N : P.range_first + blockIdx.x;
     range_taken = 1;
     return r;
   };
-  uint32_t seq = 0;
+  // pipeline: a (next to publish, record ra), b (record rb), c (claim only)
+  uint4 ra[4], rb[4];
+  uint32_t a = claim(), b = N, c = N;
+  load_record(P, a, ra);
+  if (a < N) b = claim();
+  load_record(P, b, rb);
+  if (b < N) c = claim();
+  uint32_t fs_c = 0, seq_c = 0;            // claim cursor: FIFO entry, first page of it
+  uint32_t fs_s = 0, p_s = 0, seq_s = 0;   // stream cursor: FIFO entry, page in it, ring seq
+  bool ended = false;                      // END published at entry fs_c - 1
   bool ok = true;
-  uint32_t next = claim();
-  for (uint32_t fs = 0; ok; ++fs) {
-    const uint32_t f = fs % kFifo, k = fs / kFifo;
-    if (k > 0 && !thread_wait(P, S, &S.iempty[f], (k - 1) & 1u, kWhereLoader | next)) {
-      ok = false;
-      break;
-    }
-    const uint32_t idx = next;
-    if (idx >= N) {
-      S.fifo[f].op = MK_OP_END;
-      S.meta[f].idx = N;
-      mbar_arrive(&S.ifull[f]);
-      break;
-    }
-    const uint4 *src = reinterpret_cast<const uint4 *>(P.instr + idx);
-    uint4 *dst = reinterpret_cast<uint4 *>(&S.fifo[f]);
+  uint64_t t_idle = gtimer();
+  uint32_t n_idle = 0;
+  while (true) {
+    bool progress = false;
+    // ---- claim cursor
+    if (!ended && fs_c - fs_s < P.lookahead) {
+      const uint32_t f = fs_c % kFifo, k = fs_c / kFifo;
+      if (k == 0 || mbar_test(&S.iempty[f], (k - 1) & 1u)) {
+        if (a >= N) {
+          S.fifo[f].op = MK_OP_END;
+          S.meta[f].idx = N;
+          S.meta[f].npages = 0;
+          mbar_arrive(&S.ifull[f]);
+          ended = true;
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(&S.fifo[f]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = __ldg(src + i);
-    const mk_instr in = S.fifo[f];
-    next = claim();  // the next claim overlaps this instruction's copies
-    const uint32_t np = n_pages(P, S, in);
-    SlotMeta &m = S.meta[f];
-    m.idx = idx;
-    m.seq0 = seq;
-    m.npages = np;
-    m.t_claim = (P.flags & MK_FLAG_TRACE) ? gtimer() : 0ull;
-    mbar_arrive(&S.ifull[f]);
-    for (uint32_t p = 0; p < np; ++p) {
-      const uint32_t slot = seq % E, kk = seq / E;
-      if (kk > 0 && !thread_wait(P, S, &S.empty[slot], (kk - 1) & 1u, kWhereLoader | idx)) {
+          for (int i = 0; i < 4; ++i) dst[i] = ra[i];
+          const mk_instr &in = S.fifo[f];
+          const uint32_t np = n_pages(P, S, in);
+          SlotMeta &m = S.meta[f];
+          m.idx = a;
+          m.seq0 = seq_c;
+          m.npages = np;
+          m.t_claim = (P.flags & MK_FLAG_TRACE) ? gtimer() : 0ull;
+          mbar_arrive(&S.ifull[f]);
+          seq_c += np;
+          // advance the pipeline
+          a = b;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ra[i] = rb[i];
+          b = c;
+          load_record(P, b, rb);
+          c = b < N ? claim() : N;
+        }
+        ++fs_c;
+        progress = true;
+      }
+    }
+    // ---- stream cursor
+    if (fs_s < fs_c) {
+      const uint32_t f = fs_s % kFifo;
+      const mk_instr &in = S.fifo[f];
+      if (in.op == MK_OP_END) break;  // everything before END is streamed
+      const uint32_t np = S.meta[f].npages;
+      if (p_s < np) {
+        const uint32_t slot = seq_s % E, kk = seq_s / E;
+        if (kk == 0 || mbar_test(&S.empty[slot], (kk - 1) & 1u)) {
+          const void *gsrc;
+          uint32_t bytes;
+          page_src(P, S, in, p_s, np, gsrc, bytes);
+          mbar_arrive_expect_tx(&S.full[slot], bytes);
+          bulk_g2s(S.ring + (size_t)slot * PG, gsrc, bytes, &S.full[slot], pol);
+          ++seq_s;
+          ++p_s;
+          progress = true;
+        }
+      }
+      if (p_s == np) {
+        if ((P.flags & MK_FLAG_TRACE) && np) S.meta[f].t_issued = gtimer();
+        ++fs_s;
+        p_s = 0;
+        progress = true;
+      }
+    }
+    if (progress) {
+      t_idle = gtimer();
+      n_idle = 0;
+    } else {
+      if (should_stop(P, S, t_idle, n_idle, kWhereLoader | fs_s)) {
         ok = false;
         break;
       }
-      const void *gsrc;
-      uint32_t bytes;
-      page_src(P, S, in, p, np, gsrc, bytes);
-      mbar_arrive_expect_tx(&S.full[slot], bytes);
-      bulk_g2s(S.ring + (size_t)slot * PG, gsrc, bytes, &S.full[slot], pol);
-      ++seq;
     }
-    if (P.flags & MK_FLAG_TRACE) m.t_issued = gtimer();
   }
-  if (!ok) drain_copies(P, S, seq);
+  if (!ok) drain_copies(P, S, seq_s);
 }
 
 // -------------------------------------------------------------- compute ----
@@ -403,40 +479,82 @@ DEVI void load_gain8(const uint16_t *g, int col, float (&v)[8]) {
 
 // Batch 1: the warp's input slice, normalised and scaled by the gains, kept
 // in registers for as long as consecutive instructions share the input.
-DEVI void load_input_b1(const KParams &P, const Smem &S, const mk_instr &in, uint32_t s,
-                        int lane, XCache &X) {
+// Split in two so the gains (constants) are loaded before the dependency
+// wait and only the activations are fetched after it, in one round trip.
+DEVI uint32_t input_key(const mk_instr &in) {
+  return ((uint32_t)in.op << 24) | ((uint32_t)(in.flags & 1) << 23) | in.layer;
+}
+
+DEVI void preload_gain_b1(const KParams &P, const mk_instr &in, uint32_t s, int lane,
+                          XCache &X) {
   const OpGeom &G = P.geom[in.op];
-  const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const uint16_t *gain = gain_of(P, in.op, in.layer);
-  float ss = 0.f;
+  if (!gain) return;
 #pragma unroll
   for (int j = 0; j < kMaxChunks; ++j)
-    if (j < (int)G.nch) {
-      load8(P, S, in.op, emb, 0, s * G.SW + j * 256 + lane * 8, X.v[j]);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) ss = fmaf(X.v[j][t], X.v[j][t], ss);
+    if (j < (int)G.nch) load_gain8(gain, s * G.SW + j * 256 + lane * 8, X.v[j]);
+}
+
+// Barrier of the compute warps on an mbarrier (bounded).
+DEVI bool compute_sync(const KParams &P, const Smem &S, uint64_t *bar, uint32_t &uses, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = warp_wait(P, S, bar, uses & 1u, kWhereCompute);
+  ++uses;
+  return ok;
+}
+
+// Normalised inputs (QKV, gate/up, LM head): all compute warps stage the H
+// activations of the sequence into shared memory in one round trip, each
+// adding its squares to a per-warp partial, then meet at a barrier.  The
+// staging buffer is single: the next normalised phase depends (through the
+// counters) on every instruction of this one, including this block's, so no
+// warp still reads it when the next staging starts.
+DEVI bool stage_norm_input(const KParams &P, const Smem &S, const mk_instr &in, int cw, int lane,
+                           uint32_t &xbar_uses) {
+  const uint32_t K = P.geom[in.op].K;
+  const int emb = in.op == MK_OP_QKV && (in.flags & 1);
+  float ss = 0.f;
+  for (uint32_t i = (uint32_t)(cw * 32 + lane) * 4; i < K; i += kComputeWarps * 32 * 4) {
+    float4 v;
+    if (emb) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2 *>(P.embed + (size_t)S.tok[0] * P.H + i));
+      v = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+    } else {
+      v = __ldcg(reinterpret_cast<const float4 *>(P.x + i));
     }
-  if (gain) {
-    for (uint32_t s2 = 0; s2 < G.NS; ++s2) {
-      if (s2 == s) continue;
-      for (uint32_t j = 0; j < G.nch; ++j) {
-        float t8[8];
-        load8(P, S, in.op, emb, 0, s2 * G.SW + j * 256 + lane * 8, t8);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) ss = fmaf(t8[t], t8[t], ss);
-      }
-    }
-    ss = warp_sum(ss);
+    *reinterpret_cast<float4 *>(S.xs + i) = v;
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) S.xs[K + cw] = ss;
+  return compute_sync(P, S, S.xbar, xbar_uses, lane);
+}
+
+// After the dependency: the warp's input slice into registers.  X holds the
+// gains (preloaded) for normalised inputs, which take x from shared memory.
+DEVI void finish_input_b1(const KParams &P, const Smem &S, const mk_instr &in, uint32_t s,
+                          int lane, XCache &X) {
+  const OpGeom &G = P.geom[in.op];
+  if (gain_of(P, in.op, in.layer) != nullptr) {
+    float ss = 0.f;
+    for (int w = 0; w < kComputeWarps; ++w) ss += S.xs[G.K + w];
     const float r = rsqrtf(ss / (float)G.K + P.eps);
 #pragma unroll
     for (int j = 0; j < kMaxChunks; ++j)
       if (j < (int)G.nch) {
-        float g8[8];
-        load_gain8(gain, s * G.SW + j * 256 + lane * 8, g8);
+        const float *xp = S.xs + s * G.SW + j * 256 + lane * 8;
+        const float4 a = *reinterpret_cast<const float4 *>(xp);
+        const float4 c = *reinterpret_cast<const float4 *>(xp + 4);
+        const float x8[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) X.v[j][t] *= r * g8[t];
+        for (int t = 0; t < 8; ++t) X.v[j][t] = x8[t] * r * X.v[j][t];
       }
+    return;
   }
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j)
+    if (j < (int)G.nch) load8(P, S, in.op, 0, 0, s * G.SW + j * 256 + lane * 8, X.v[j]);
 }
 
 DEVI float dot_item_b1(const uint8_t *item, const XCache &X, int nch, int lane) {
@@ -489,23 +607,25 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
 // Batch-1 GEMV of one instruction; X holds the normalised input slice when
 // xkey matches the instruction's input.
 DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
-                  float *res, int cw, int lane, XCache &X, uint32_t &xkey) {
+                  float *res, int cw, int lane, XCache &X, bool reload) {
   const OpGeom &G = P.geom[in.op];
   const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
   const uint32_t items = wrows * G.NS;
   const uint32_t A = G.NS * (kComputeWarps / G.NS);
   const bool active = (uint32_t)cw < A;
   const uint32_t s = cw % G.NS;
-  const uint32_t key = ((uint32_t)in.op << 24) | ((uint32_t)(in.flags & 1) << 23) | in.layer;
-  if (key != xkey) {
-    if (active) load_input_b1(P, S, in, s, lane, X);
-    xkey = key;
-  }
+  if (reload && active) finish_input_b1(P, S, in, s, lane, X);
+  // trace stamps (compute warp 0): input in registers, first and last page present
+  const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
+  SlotMeta &mw = const_cast<SlotMeta &>(meta);  // meta is this entry's slot in shared memory
+  if (stamp) mw.t_input = gtimer();
   const uint32_t E = P.ring_pages;
   uint32_t item = cw;
   for (uint32_t p = 0; p < meta.npages; ++p) {
     const uint32_t seq = meta.seq0 + p, slot = seq % E;
     if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    if (stamp && p == 0) mw.t_page0 = gtimer();
+    if (stamp && p + 1 == meta.npages) mw.t_pagel = gtimer();
     const uint8_t *page = S.ring + (size_t)slot * P.page_bytes;
     const uint32_t it_end = min(items, (p + 1) * G.ipp);
     for (; active && item < it_end; item += A) {
@@ -531,7 +651,7 @@ __device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_i
   const uint32_t A = G.NS * (kComputeWarps / G.NS);
   const bool active = (uint32_t)cw < A;
   const uint32_t s = cw % G.NS;
-  const uint32_t key = ((uint32_t)in.op << 24) | ((uint32_t)(in.flags & 1) << 23) | in.layer;
+  const uint32_t key = input_key(in);
   const int B = P.B;
   if (key != xkey) {
     ++key_changes;
@@ -585,15 +705,6 @@ __device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_i
     if (lane == 0) mbar_arrive(&S.empty[slot]);
   }
   return true;
-}
-
-// Barrier of the compute warps on an mbarrier (bounded).
-DEVI bool compute_sync(const KParams &P, const Smem &S, uint64_t *bar, uint32_t &uses, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-  const bool ok = warp_wait(P, S, bar, uses & 1u, kWhereCompute);
-  ++uses;
-  return ok;
 }
 
 // One split-KV attention chunk for the QPG query heads of group g of
@@ -799,15 +910,24 @@ DEVI void finish_entry(const KParams &P, const Smem &S, uint32_t fs, int cw, int
 // Batch-1 run of consecutive GEMV instructions sharing the register input
 // cache; returns at the first attention or end entry (not consumed).
 DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t epoch, int cw,
-                      int lane) {
+                      int lane, uint32_t &xbar_uses) {
   XCache X;
   uint32_t xkey = 0xFFFFFFFFu;
   while (true) {
     const uint32_t f = fs % kFifo;
     const mk_instr &in = S.fifo[f];
     const SlotMeta &meta = S.meta[f];
+    const uint32_t key = input_key(in);
+    const bool reload = key != xkey;
+    const uint32_t ns = P.geom[in.op].NS;
+    if (reload && (uint32_t)cw < ns * (kComputeWarps / ns))
+      preload_gain_b1(P, in, cw % ns, lane, X);
+    xkey = key;
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return false;
-    if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, xkey))
+    if (reload && gain_of(P, in.op, in.layer) != nullptr &&
+        !stage_norm_input(P, S, in, cw, lane, xbar_uses))
+      return false;
+    if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, reload))
       return false;
     finish_entry(P, S, fs, cw, lane);
     ++fs;
@@ -830,7 +950,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       return;
     }
     if (in.op != MK_OP_ATTN && P.B == 1) {
-      if (!run_gemv_b1(P, S, fs, epoch, cw, lane)) return;
+      if (!run_gemv_b1(P, S, fs, epoch, cw, lane, xbar_uses)) return;
       continue;
     }
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return;
@@ -896,14 +1016,10 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
     }
     case MK_OP_OPROJ:
     case MK_OP_DOWN: {
+      // residual rows were prefetched into rbuf by this lane (same u mapping)
       for (int u = lane; u < (int)in.nrows * B; u += 32) {
         const int r = u % in.nrows, b = u / in.nrows;
-        const int row = in.row0 + r;
-        float *xp = P.x + (size_t)b * P.H + row;
-        const float resid = (in.op == MK_OP_OPROJ && (in.flags & 1))
-                                ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
-                                : __ldcg(xp);
-        *xp = resid + val(r, b);
+        P.x[(size_t)b * P.H + in.row0 + r] = S.rbuf[u] + val(r, b);
       }
       break;
     }
@@ -939,26 +1055,45 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
     __syncwarp();
     old = __shfl_sync(0xFFFFFFFFu, old, 0);
     if (old == epoch * in.nchunk + in.nchunk - 1u) {
-      // last chunk of (b, g): merge the chunk partials by log-sum-exp
-      const int qpg = P.qpg, PS = 2 * qpg + qpg * d, per = qpg * d / 32;
+      // last chunk of (b, g): merge the chunk partials by log-sum-exp; each
+      // lane owns 8 consecutive outputs and loads four chunks at a time
+      const int qpg = P.qpg, PS = 2 * qpg + qpg * d, nout = qpg * d;
       const float *pb = P.part + ((size_t)in.b * P.nkv + in.g) * P.nchunk * PS;
-      const int o0 = lane * per, h = o0 / d, dim0 = o0 % d;
-      float M = -INFINITY, den = 0.f, num[32];
-      for (int k = 0; k < per; ++k) num[k] = 0.f;
-      for (uint32_t c = 0; c < in.nchunk; ++c) {
-        const float *pc = pb + (size_t)c * PS;
-        const float mc = __ldcg(pc + h);
-        if (mc == -INFINITY) continue;
-        const float lc = __ldcg(pc + qpg + h);
-        const float Mn = fmaxf(M, mc);
-        const float a = __expf(M - Mn), w = __expf(mc - Mn);
-        den = den * a + w * lc;
-        for (int k = 0; k < per; ++k) num[k] = num[k] * a + w * __ldcg(pc + 2 * qpg + h * d + dim0 + k);
-        M = Mn;
+      for (int o0 = lane * 8; o0 < nout; o0 += 256) {
+        const int h = o0 / d, dim0 = o0 % d;
+        float M = -INFINITY, den = 0.f, num[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) num[k] = 0.f;
+        for (uint32_t c0 = 0; c0 < in.nchunk; c0 += 4) {
+          float mc[4], lc[4], oc[4][8];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            mc[u] = -INFINITY;
+            lc[u] = 0.f;
+            if (c0 + u < in.nchunk) {
+              const float *pc = pb + (size_t)(c0 + u) * PS;
+              mc[u] = __ldcg(pc + h);
+              lc[u] = __ldcg(pc + qpg + h);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) oc[u][k] = __ldcg(pc + 2 * qpg + h * d + dim0 + k);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (mc[u] == -INFINITY) continue;
+            const float Mn = fmaxf(M, mc[u]);
+            const float a = __expf(M - Mn), w = __expf(mc[u] - Mn);
+            den = den * a + w * lc[u];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) num[k] = num[k] * a + w * oc[u][k];
+            M = Mn;
+          }
+        }
+        float *out = P.attn + (size_t)in.b * P.nq * d + ((size_t)in.g * qpg + h) * d + dim0;
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) out[k] = num[k] * inv;
       }
-      float *out = P.attn + (size_t)in.b * P.nq * d + ((size_t)in.g * qpg + h) * d + dim0;
-      const float inv = 1.f / den;
-      for (int k = 0; k < per; ++k) out[k] = num[k] * inv;
       fence_gpu();
       __syncwarp();
       if (lane == 0) red_add(ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
@@ -975,7 +1110,26 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
       tr[4] = meta.t_issued;
       tr[5] = meta.t_cdone;
       tr[6] = meta.t_sstart;
-      tr[7] = 0;
+      tr[7] = meta.t_input;
+      tr[8] = meta.t_page0;
+      tr[9] = meta.t_pagel;
+    }
+  }
+}
+
+// Residual rows of an O/down instruction, fetched while the compute warps
+// work on it (its input counter is satisfied once the slot is ready).
+DEVI void prefetch_residual(const KParams &P, const Smem &S, const mk_instr &in, int lane) {
+  if (in.op != MK_OP_OPROJ && in.op != MK_OP_DOWN) return;
+  const int n = (int)in.nrows * P.B;
+#pragma unroll
+  for (int i = 0; i < kMaxItems * kMaxBatch / 32; ++i) {
+    const int u = lane + 32 * i;
+    if (u < n) {
+      const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
+      S.rbuf[u] = (in.op == MK_OP_OPROJ && (in.flags & 1))
+                      ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
+                      : __ldcg(P.x + (size_t)b * P.H + row);
     }
   }
 }
@@ -983,10 +1137,13 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
 DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
   for (uint32_t fs = 0;; ++fs) {
     const uint32_t f = fs % kFifo, k = fs / kFifo;
-    if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
+    if (!warp_wait(P, S, &S.ifull[f], k & 1u, kWhereStorer)) break;
     const mk_instr &in = S.fifo[f];
     const SlotMeta &meta = S.meta[f];
     if (in.op == MK_OP_END) break;
+    if (!warp_wait(P, S, &S.rdy[f], k & 1u, kWhereStorer)) break;
+    prefetch_residual(P, S, in, lane);
+    if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
     if (lane == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[f].t_sstart = gtimer();
     __syncwarp();
     storer_epilogue(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);

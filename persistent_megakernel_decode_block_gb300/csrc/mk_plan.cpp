@@ -56,7 +56,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) REJECT("rms_eps >= 0 and rope_theta > 0 required");
   if (c.sched_mode != MK_SCHED_DYNAMIC && c.sched_mode != MK_SCHED_STATIC) REJECT("bad sched_mode");
   if (num_sms < 1 || num_sms > 1024) REJECT("number of SMs out of range");
-  const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : 16384u;
+  const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : 32768u;
   if (page < 4096 || page > 65536 || page % 1024) REJECT("page_bytes must be a multiple of 1024 in 4096..65536");
 
   P = HostPlan();
@@ -334,6 +334,8 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_rope = take(B * d * 4, 16);
   uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
   uint32_t rel_misc = take(64, 16);
+  uint32_t rel_rbuf = take(kMaxItems * kMaxBatch * 4, 16);  // storer's prefetched residuals
+  uint32_t rel_xs = take((H + kComputeWarps) * 4, 16);        // staged normalised input
   uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 2) * 8;
   uint32_t rel_bars = take(bars_max, 8);
   uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
@@ -350,6 +352,8 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.off_rope = ring + rel_rope;
   P.off_normr = ring + rel_normr;
   P.off_misc = ring + rel_misc;
+  P.off_rbuf = ring + rel_rbuf;
+  P.off_xs = ring + rel_xs;
   P.off_bars = ring + rel_bars;
   P.smem_total = ring + fixed;
   if (P.smem_total > smem_limit) REJECT("shared-memory layout exceeds the limit");

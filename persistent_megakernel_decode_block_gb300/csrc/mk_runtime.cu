@@ -197,6 +197,9 @@ static int setup_device(mk_plan_s *p) {
   P.n_blocks = H.num_sms;
   P.flags = c.flags;
   P.timeout_ns = (uint64_t)(c.wait_timeout_us > 0 ? c.wait_timeout_us : 1000000) * 1000ull;
+  // static lists may run a full FIFO ahead; the dynamic queue claims close
+  // to need so the claims still balance the blocks
+  P.lookahead = P.mode == kModeStatic ? (uint32_t)kFifo : 3u;
   P.ring_pages = H.ring_pages;
   P.page_bytes = H.page_bytes;
   P.off_bars = H.off_bars;
@@ -210,6 +213,8 @@ static int setup_device(mk_plan_s *p) {
   P.off_rope = H.off_rope;
   P.off_normr = H.off_normr;
   P.off_misc = H.off_misc;
+  P.off_rbuf = H.off_rbuf;
+  P.off_xs = H.off_xs;
   P.smem_total = H.smem_total;
   return MK_OK;
 }

@@ -269,7 +269,7 @@ def mk_read_counters(plan):
 
 def mk_read_trace(plan):
     info = mk_plan_info(plan)
-    tr = np.zeros((info["n_instr"], 8), np.uint64)
+    tr = np.zeros((info["n_instr"], 10), np.uint64)
     _check(lib().mk_read_trace(plan, tr.ctypes.data), "mk_read_trace")
     return tr
 
