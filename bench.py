@@ -42,7 +42,7 @@ def args_():
     p.add_argument("--impl", default="mine", choices=["mine", "reference"])
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--sched", default="dynamic", choices=["dynamic", "static"])
+    p.add_argument("--sched", default="static", choices=["dynamic", "static"])
     p.add_argument("--no-baselines", action="store_true", help="skip multi-kernel and CPU legs")
     p.add_argument("--trace", default="", help="write a per-instruction trace (npz) here")
     return p.parse_args()

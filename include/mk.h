@@ -89,6 +89,9 @@ typedef struct mk_config {
   int32_t smem_bytes;      /* 0 -> device opt-in maximum per block */
   int32_t page_bytes;      /* shared-memory page size; 0 -> 32768 */
   int32_t attn_chunk;      /* max KV positions per attention instruction; 0 -> auto */
+  int32_t l2_prefetch_kb;  /* per block: KB of published pages prefetched into L2 ahead of
+                              the shared-memory ring; <= 0 -> none (the default: on the
+                              batch-1 workloads the extra L2 traffic costs more than it hides) */
 } mk_config;
 
 /* One instruction: a fixed 64-byte little-endian record.

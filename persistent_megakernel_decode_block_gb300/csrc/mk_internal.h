@@ -19,6 +19,9 @@ constexpr int kMaxItems = 32;   // work items (row x slice) per GEMV instruction
 constexpr int kMaxChunks = 8;   // 256-column chunks per item (registers per lane / 8)
 constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
 constexpr int kMaxRing = 32;
+// block flags (bail, bad input) at the start of the misc area, then the
+// table of the block's shared-memory pointers
+constexpr int kMiscDescOffset = 64, kMiscDescBytes = 256;
 
 // control words (u32 index into the ctrl block)
 constexpr int kCtlStatus = 0, kCtlWhere = 1, kCtlAbort = 2, kCtlEpoch = 3;
@@ -52,12 +55,14 @@ struct KParams {
   const float *rope_cos, *rope_sin;  // [max_ctx][d/2]
   OpGeom geom[8];
   int32_t L, H, nq, nkv, d, F, V, B, max_ctx, qpg;
-  int32_t nchunk, attn_chunk;
+  int32_t nchunk, attn_chunk, att_lmax;
   float eps, attn_scale;
   int32_t n_wait, mode;
   uint32_t range_first, range_count, n_blocks, flags;
-  uint64_t timeout_ns;
+  uint64_t timeout_cycles;  // wait limit in SM cycles (at the maximum SM clock)
   uint32_t lookahead;  // FIFO entries the loader may publish ahead of its stream
+  uint32_t l2_window;  // bytes of published pages prefetched into L2 ahead of the ring
+  uint32_t loader_idle_ns;  // back-off of the loader thread when it can make no progress
   // dynamic shared-memory layout (byte offsets)
   uint32_t ring_pages, page_bytes;
   uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,

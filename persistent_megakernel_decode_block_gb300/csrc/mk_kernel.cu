@@ -69,6 +69,10 @@ DEVI bool mbar_test(uint64_t *b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// bulk prefetch of global memory into L2 (no shared memory, no completion)
+DEVI void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 DEVI uint64_t policy_evict_first() {
   uint64_t p;
@@ -102,6 +106,9 @@ DEVI uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
   return old;
 }
 DEVI void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// SM cycle counter: cheap to read, used for every wait limit (the limits are
+// budgeted at the maximum SM clock, so a limit is never shorter than stated)
+DEVI uint64_t cycles() { return (uint64_t)clock64(); }
 DEVI uint64_t gtimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -133,11 +140,13 @@ struct Smem {
   uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar;
   mk_instr *fifo;
   SlotMeta *meta;
-  float *res, *att_s, *opart, *lpart, *rope, *normr, *rbuf, *xs;
+  float *res, *opart, *ml, *sc, *rope, *normr, *rbuf, *xs;
   uint32_t *sat;
   int32_t *pos, *tok;
   volatile int *misc;  // [0] bail, [1] bad input
 };
+
+static_assert(sizeof(Smem) <= kMiscDescBytes, "pointer table larger than its slot");
 
 DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   Smem S;
@@ -155,9 +164,9 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.fifo = reinterpret_cast<mk_instr *>(base + P.off_fifo);
   S.meta = reinterpret_cast<SlotMeta *>(base + P.off_meta);
   S.res = reinterpret_cast<float *>(base + P.off_res);
-  S.att_s = reinterpret_cast<float *>(base + P.off_att);
-  S.opart = S.att_s + P.qpg * P.attn_chunk;
-  S.lpart = S.opart + kComputeWarps * P.d;
+  S.opart = reinterpret_cast<float *>(base + P.off_att);  // [2][warp][d]
+  S.ml = S.opart + 2 * kComputeWarps * P.d;                  // [2][warp][m, l]
+  S.sc = S.ml + 2 * kComputeWarps * 2;                       // [warp][att_lmax]
   S.sat = reinterpret_cast<uint32_t *>(base + P.off_sat);
   S.pos = reinterpret_cast<int32_t *>(base + P.off_pos);
   S.tok = S.pos + kMaxBatch;
@@ -187,7 +196,7 @@ DEVI bool should_stop(const KParams &P, const Smem &S, uint64_t t0, uint32_t &n,
       S.misc[0] = 1;
       return true;
     }
-    if (gtimer() - t0 > P.timeout_ns) {
+    if (cycles() - t0 > P.timeout_cycles) {
       raise_error(P, MK_ERR_TIMEOUT, where, true);
       S.misc[0] = 1;
       return true;
@@ -200,7 +209,7 @@ DEVI bool should_stop(const KParams &P, const Smem &S, uint64_t t0, uint32_t &n,
 DEVI bool thread_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity,
                       uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
+  const uint64_t t0 = cycles();
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity))
     if (should_stop(P, S, t0, n, where)) return false;
@@ -212,7 +221,7 @@ DEVI bool thread_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t p
 DEVI bool warp_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t parity,
                     uint32_t where) {
   if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
-  const uint64_t t0 = gtimer();
+  const uint64_t t0 = cycles();
   uint32_t n = 0;
   while (true) {
     if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
@@ -279,9 +288,9 @@ DEVI void drain_copies(const KParams &P, const Smem &S, uint32_t seq) {
   for (uint32_t s = first; s < seq; ++s) {
     uint64_t *bar = &S.full[s % E];
     const uint32_t par = (s / E) & 1u;
-    const uint64_t t0 = gtimer();
+    const uint64_t t0 = cycles();
     while (!mbar_try_wait(bar, par))
-      if (gtimer() - t0 > 200000000ull) {  // 200 ms: a bulk copy never takes that long
+      if (cycles() - t0 > 500000000ull) {  // >= 200 ms: a bulk copy never takes that long
         raise_error(P, MK_ERR_TIMEOUT, kWhereDrain | s, true);
         break;
       }
@@ -333,9 +342,10 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   if (b < N) c = claim();
   uint32_t fs_c = 0, seq_c = 0;            // claim cursor: FIFO entry, first page of it
   uint32_t fs_s = 0, p_s = 0, seq_s = 0;   // stream cursor: FIFO entry, page in it, ring seq
+  uint32_t fs_p = 0, p_p = 0, seq_p = 0;   // L2-prefetch cursor (never behind the stream)
   bool ended = false;                      // END published at entry fs_c - 1
   bool ok = true;
-  uint64_t t_idle = gtimer();
+  uint64_t t_idle = 0;  // start of the current idle stretch (0: not idle)
   uint32_t n_idle = 0;
   while (true) {
     bool progress = false;
@@ -374,6 +384,31 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
         progress = true;
       }
     }
+    // ---- L2-prefetch cursor: up to l2_window bytes of published pages ahead
+    // of the ring, so pages the ring cannot hold yet are near when it can
+    if (seq_p < seq_s) {  // caught up by the stream: restart at its position
+      fs_p = fs_s;
+      p_p = p_s;
+      seq_p = seq_s;
+    }
+    if (P.l2_window && fs_p < fs_c && (uint64_t)(seq_p - seq_s) * PG < P.l2_window) {
+      const uint32_t f = fs_p % kFifo;
+      const mk_instr &in = S.fifo[f];
+      const uint32_t np = in.op == MK_OP_END ? 0u : S.meta[f].npages;
+      if (p_p < np) {
+        const void *gsrc;
+        uint32_t bytes;
+        page_src(P, S, in, p_p, np, gsrc, bytes);
+        bulk_prefetch_l2(gsrc, bytes);
+        ++p_p;
+        ++seq_p;
+        progress = true;
+      }
+      if (p_p >= np && in.op != MK_OP_END) {
+        ++fs_p;
+        p_p = 0;
+      }
+    }
     // ---- stream cursor
     if (fs_s < fs_c) {
       const uint32_t f = fs_s % kFifo;
@@ -401,9 +436,12 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
       }
     }
     if (progress) {
-      t_idle = gtimer();
+      t_idle = 0;
       n_idle = 0;
     } else {
+      if (!t_idle) t_idle = cycles() | 1u;
+      // idle: yield the sub-partition's issue slots to the compute warps on it
+      __nanosleep(P.loader_idle_ns);
       if (should_stop(P, S, t_idle, n_idle, kWhereLoader | fs_s)) {
         ok = false;
         break;
@@ -428,7 +466,7 @@ DEVI bool poll_counter(const KParams &P, const Smem &S, const mk_instr &in, uint
   const uint32_t *p = P.ctr + (size_t)c * kCtrStride;
   bool ok = (int32_t)(ld_acquire(p) - target) >= 0;
   if (!ok) {
-    const uint64_t t0 = gtimer();
+    const uint64_t t0 = cycles();
     uint32_t n = 0;
     while (true) {
       __nanosleep(20);
@@ -504,16 +542,21 @@ DEVI bool compute_sync(const KParams &P, const Smem &S, uint64_t *bar, uint32_t 
   return ok;
 }
 
-// Normalised inputs (QKV, gate/up, LM head): all compute warps stage the H
-// activations of the sequence into shared memory in one round trip, each
+// Normalised inputs (QKV, gate/up, LM head) and the O-projection's input:
+// all compute warps stage the K activations of the sequence into shared memory in one round trip, each
 // adding its squares to a per-warp partial, then meet at a barrier.  The
 // staging buffer is single: the next normalised phase depends (through the
 // counters) on every instruction of this one, including this block's, so no
 // warp still reads it when the next staging starts.
-DEVI bool stage_norm_input(const KParams &P, const Smem &S, const mk_instr &in, int cw, int lane,
-                           uint32_t &xbar_uses) {
+DEVI bool stages_input(const KParams &P, const mk_instr &in) {
+  return in.op == MK_OP_OPROJ || gain_of(P, in.op, in.layer) != nullptr;
+}
+
+DEVI bool stage_input(const KParams &P, const Smem &S, const mk_instr &in, int cw, int lane,
+                      uint32_t &xbar_uses) {
   const uint32_t K = P.geom[in.op].K;
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
+  const float *src = in.op == MK_OP_OPROJ ? P.attn : P.x;
   float ss = 0.f;
   for (uint32_t i = (uint32_t)(cw * 32 + lane) * 4; i < K; i += kComputeWarps * 32 * 4) {
     float4 v;
@@ -521,7 +564,7 @@ DEVI bool stage_norm_input(const KParams &P, const Smem &S, const mk_instr &in, 
       const uint2 w = __ldg(reinterpret_cast<const uint2 *>(P.embed + (size_t)S.tok[0] * P.H + i));
       v = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
     } else {
-      v = __ldcg(reinterpret_cast<const float4 *>(P.x + i));
+      v = __ldcg(reinterpret_cast<const float4 *>(src + i));
     }
     *reinterpret_cast<float4 *>(S.xs + i) = v;
     ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
@@ -549,6 +592,18 @@ DEVI void finish_input_b1(const KParams &P, const Smem &S, const mk_instr &in, u
         const float x8[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
         for (int t = 0; t < 8; ++t) X.v[j][t] = x8[t] * r * X.v[j][t];
+      }
+    return;
+  }
+  if (in.op == MK_OP_OPROJ) {  // staged, no norm
+#pragma unroll
+    for (int j = 0; j < kMaxChunks; ++j)
+      if (j < (int)G.nch) {
+        const float *xp = S.xs + s * G.SW + j * 256 + lane * 8;
+        const float4 a = *reinterpret_cast<const float4 *>(xp);
+        const float4 c = *reinterpret_cast<const float4 *>(xp + 4);
+        X.v[j][0] = a.x; X.v[j][1] = a.y; X.v[j][2] = a.z; X.v[j][3] = a.w;
+        X.v[j][4] = c.x; X.v[j][5] = c.y; X.v[j][6] = c.z; X.v[j][7] = c.w;
       }
     return;
   }
@@ -708,167 +763,224 @@ __device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_i
 }
 
 // One split-KV attention chunk for the QPG query heads of group g of
-// sequence b: scores q.k/sqrt(d) over the chunk's positions, then the
-// chunk's max m, denominator l = sum exp(s - m) and unnormalised output
-// sum exp(s - m) v, written to the slot's result area as {m[QPG], l[QPG],
-// o[QPG][D]}.  Keys/values of positions below p_b come from the ring
-// pages; the one at p_b (written this step) from global memory.
+// sequence b over its positions [p0, p1): scores q.k/sqrt(d), the chunk's
+// maximum m, denominator l = sum exp(s - m) and unnormalised output
+// o = sum exp(s - m) v, written to the partials buffer as {m[QPG], l[QPG],
+// o[QPG][D]} (the paper's split-KV decode attention; chunks are merged by
+// log-sum-exp once all of a group's chunks are in).
+//
+// Keys and values of the positions below p_b arrive as one ring page each;
+// the key and value of p_b itself (written this step) are read from global
+// memory.  Warp cw serves head cw % QPG over a contiguous share of the
+// chunk: it keeps its scores in its own shared-memory row, so the warps meet
+// only once, to merge the per-warp partials of each head.
 template <int D, int QPG>
-__device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
-                     float *res, int cw, int lane, uint32_t &att_uses) {
-  constexpr int LPP = D / 8;       // lanes per key row (16 bytes each)
-  constexpr int PPW = 32 / LPP;    // key rows per warp step
-  constexpr int T = kComputeWarps * PPW;
-  constexpr int DPL = D / 32;      // value dims per lane
+__device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const mk_instr &in,
+                                        const SlotMeta &meta, int cw, int lane,
+                                        uint32_t &att_uses) {
+  constexpr int LPP = D / 8;      // lanes per key row (16 bytes each)
+  constexpr int RPS = 32 / LPP;   // key rows per warp step
+  constexpr int DPL = D / 32;     // value dims per lane
   const int b = in.b, g = in.g, pos = S.pos[b];
   int p0, p1;
   attn_range(pos, in.nchunk, in.chunk, p0, p1);
   const int n_tot = p1 - p0;
-  const int n_old = max(0, min(p1, pos) - p0);
-  const int rpp = P.page_bytes / (D * 2);
-  const int npk = (n_old + rpp - 1) / rpp;
-  const int CH = P.attn_chunk;
+  const int n_old = max(0, min(p1, pos) - p0);  // rows that come from the ring
   const uint32_t E = P.ring_pages;
-  float *s_buf = S.att_s;
-  const int part = lane % LPP, t = cw * PPW + lane / LPP;
-  const float scale = P.attn_scale;
+  const int h = cw % QPG, r = cw / QPG;
+  const int nqs = (kComputeWarps - 1 - h) / QPG + 1;  // warps serving head h
+  const int len = (n_tot + nqs - 1) / nqs;
+  const int j0 = min(r * len, n_tot), j1 = min(j0 + len, n_tot);
+  const int part = lane % LPP;
+  const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
+  SlotMeta &mw = const_cast<SlotMeta &>(meta);  // this entry's slot in shared memory
 
-  float q[QPG][8];
+  // query slice of head h (8 dims per lane), pre-scaled by 1/sqrt(d); the
+  // current position's key slice and value dims if this warp covers p_b
+  float q8[8], kn8[8], vn[DPL];
   {
-    const float *qb = P.q + ((size_t)b * P.nq + (size_t)g * QPG) * D + part * 8;
+    const float *qh = P.q + ((size_t)b * P.nq + (size_t)g * QPG + h) * D + part * 8;
+    const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(qh));
+    const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(qh + 4));
+    const float sc = P.attn_scale;
+    q8[0] = x0.x * sc; q8[1] = x0.y * sc; q8[2] = x0.z * sc; q8[3] = x0.w * sc;
+    q8[4] = x1.x * sc; q8[5] = x1.y * sc; q8[6] = x1.z * sc; q8[7] = x1.w * sc;
 #pragma unroll
-    for (int h = 0; h < QPG; ++h) {
-      const float4 a = __ldcg(reinterpret_cast<const float4 *>(qb + h * D));
-      const float4 c = __ldcg(reinterpret_cast<const float4 *>(qb + h * D + 4));
-      q[h][0] = a.x; q[h][1] = a.y; q[h][2] = a.z; q[h][3] = a.w;
-      q[h][4] = c.x; q[h][5] = c.y; q[h][6] = c.z; q[h][7] = c.w;
+    for (int u = 0; u < 8; ++u) kn8[u] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) vn[k] = 0.f;
+    if (n_old >= j0 && n_old < j1) {
+      const size_t at = kv_row(P, in.layer, b, g, pos);
+      const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(P.kc + at + part * 8));
+      kn8[0] = bf_lo(w.x); kn8[1] = bf_hi(w.x); kn8[2] = bf_lo(w.y); kn8[3] = bf_hi(w.y);
+      kn8[4] = bf_lo(w.z); kn8[5] = bf_hi(w.z); kn8[6] = bf_lo(w.w); kn8[7] = bf_hi(w.w);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) vn[k] = bf1(__ldcg(P.vc + at + lane * DPL + k));
     }
   }
-  auto score_rows = [&](const uint8_t *rows, const uint16_t *grow, int a, int e) {
-    for (int jj = a - (a % T); jj < e; jj += T) {
-      const int j = jj + t;
-      const bool valid = j >= a && j < e;
-      uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) {
-        if (rows) w = *reinterpret_cast<const uint4 *>(rows + (size_t)(j - a) * D * 2 + part * 16);
-        else w = __ldcg(reinterpret_cast<const uint4 *>(grow + part * 8));
+  if (stamp) mw.t_input = gtimer();
+  const bool paged = n_old > 0;  // one key page and one value page
+  const uint8_t *kpage = S.ring + (size_t)(meta.seq0 % E) * P.page_bytes;
+  const uint8_t *vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
+  if (paged && !warp_wait(P, S, &S.full[meta.seq0 % E], (meta.seq0 / E) & 1u, kWhereCompute | meta.idx))
+    return false;
+  if (stamp) mw.t_page0 = gtimer();
+
+  // 1. scores of rows j0..j1 into this warp's row of S.sc
+  float *sw = S.sc + (size_t)cw * P.att_lmax;
+#pragma unroll 2
+  for (int jb = j0; jb < j1; jb += RPS) {
+    const int j = jb + lane / LPP;
+    float dsum = 0.f;
+    if (j < j1) {
+      float k8[8];
+      if (j < n_old) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(kpage + (size_t)j * D * 2 + part * 16);
+        k8[0] = bf_lo(w.x); k8[1] = bf_hi(w.x); k8[2] = bf_lo(w.y); k8[3] = bf_hi(w.y);
+        k8[4] = bf_lo(w.z); k8[5] = bf_hi(w.z); k8[6] = bf_lo(w.w); k8[7] = bf_hi(w.w);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) k8[u] = kn8[u];
       }
-      const float k8[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                           bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int h = 0; h < QPG; ++h) {
-        float dsum = 0.f;
+      for (int u = 0; u < 8; u += 2) {
+        a0 = fmaf(q8[u], k8[u], a0);
+        a1 = fmaf(q8[u + 1], k8[u + 1], a1);
+      }
+      dsum = a0 + a1;
+    }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) dsum = fmaf(q[h][u], k8[u], dsum);
+    for (int o = LPP / 2; o; o >>= 1) dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
+    if (part == 0 && j < j1) sw[j - j0] = dsum;
+  }
+  __syncwarp();
+
+  // 2. this warp's maximum, probabilities and denominator
+  const int cnt = j1 - j0;
+  float mx = -INFINITY;
+  for (int i = lane; i < cnt; i += 32) mx = fmaxf(mx, sw[i]);
+  const float m = warp_max(mx);
+  float lsum = 0.f;
+  for (int i = lane; i < cnt; i += 32) {
+    const float pj = __expf(sw[i] - m);
+    sw[i] = pj;
+    lsum += pj;
+  }
+  const float l = warp_sum(lsum);
+  __syncwarp();
+
+  // 3. o = sum_j p_j v_j over this warp's rows; lanes own DPL dims each
+  if (paged && !warp_wait(P, S, &S.full[(meta.seq0 + 1) % E], ((meta.seq0 + 1) / E) & 1u,
+                          kWhereCompute | meta.idx))
+    return false;
+  float o[4][DPL];
 #pragma unroll
-        for (int o = LPP / 2; o; o >>= 1) dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
-        if (valid && part == 0) s_buf[h * CH + j] = dsum * scale;
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) o[u][k] = 0.f;
+  const int jo = min(j1, n_old);  // rows of this warp that come from the value page
+  const uint8_t *vrow = vpage + lane * DPL * 2;
+  int j = j0;
+  for (; j + 4 <= jo; j += 4) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float pj = sw[j + u - j0];
+      const uint8_t *row = vrow + (size_t)(j + u) * D * 2;
+      if constexpr (DPL == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(row);
+        o[u][0] = fmaf(pj, bf_lo(w), o[u][0]);
+        o[u][1] = fmaf(pj, bf_hi(w), o[u][1]);
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2 *>(row);
+        o[u][0] = fmaf(pj, bf_lo(w.x), o[u][0]);
+        o[u][1] = fmaf(pj, bf_hi(w.x), o[u][1]);
+        o[u][DPL > 2 ? 2 : 0] = fmaf(pj, bf_lo(w.y), o[u][DPL > 2 ? 2 : 0]);
+        o[u][DPL > 2 ? 3 : 1] = fmaf(pj, bf_hi(w.y), o[u][DPL > 2 ? 3 : 1]);
       }
     }
-  };
-  // scores: K pages, then the new key
-  for (int p = 0; p < npk; ++p) {
-    const uint32_t seq = meta.seq0 + p, slot = seq % E;
-    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
-    const int a = p * rpp, e = min(n_old, a + rpp);
-    score_rows(S.ring + (size_t)slot * P.page_bytes, nullptr, a, e);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
   }
-  if (n_tot > n_old) score_rows(nullptr, P.kc + kv_row(P, in.layer, b, g, pos), n_old, n_tot);
+  for (; j < j1; ++j) {
+    const float pj = sw[j - j0];
+    if (j < n_old) {
+      const uint8_t *row = vrow + (size_t)j * D * 2;
+#pragma unroll
+      for (int k = 0; k < DPL; k += 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(row + k * 2);
+        o[0][k] = fmaf(pj, bf_lo(w), o[0][k]);
+        o[0][k + 1] = fmaf(pj, bf_hi(w), o[0][k + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[0][k] = fmaf(pj, vn[k], o[0][k]);
+    }
+  }
+  // every warp is done with the chunk's pages
+  __syncwarp();
+  if (paged && lane == 0) {
+    mbar_arrive(&S.empty[meta.seq0 % E]);
+    mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
+  }
+  if (stamp) mw.t_pagel = gtimer();
+
+  // 4. per-warp partials (double-buffered by instruction parity: a warp can
+  //    be at most one instruction ahead of the warps merging the last one)
+  const uint32_t par = att_uses & 1u;
+  float *op = S.opart + (size_t)par * kComputeWarps * D;
+  float *mlp = S.ml + par * kComputeWarps * 2;
+#pragma unroll
+  for (int k = 0; k < DPL; ++k)
+    op[cw * D + lane * DPL + k] = (o[0][k] + o[1][k]) + (o[2][k] + o[3][k]);
+  if (lane == 0) {
+    mlp[cw * 2] = m;
+    mlp[cw * 2 + 1] = l;
+  }
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
 
-  // per-head maximum (every warp computes the same values)
-  float m[QPG];
+  // 5. warp hh < QPG merges the partials of head hh into the chunk partial
+  if (cw < QPG) {
+    float M = -INFINITY;
+    for (int w = cw; w < kComputeWarps; w += QPG) M = fmaxf(M, mlp[w * 2]);
+    float L = 0.f, acc[DPL];
 #pragma unroll
-  for (int h = 0; h < QPG; ++h) {
-    float mx = -INFINITY;
-    for (int j = lane; j < n_tot; j += 32) mx = fmaxf(mx, s_buf[h * CH + j]);
-    m[h] = warp_max(mx);
-  }
-  // p = exp(s - m) against V rows: warp cw -> head hh = cw % QPG, position
-  // subset qs = cw / QPG of the nqs(hh) warps that serve that head
-  const int hh = cw % QPG, qs = cw / QPG;
-  const int NQS = (kComputeWarps - 1 - hh) / QPG + 1;
-  float o[DPL];
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    if (M != -INFINITY) {
+      for (int w = cw; w < kComputeWarps; w += QPG) {
+        const float mw_ = mlp[w * 2];
+        if (mw_ == -INFINITY) continue;
+        const float a = __expf(mw_ - M);
+        L = fmaf(a, mlp[w * 2 + 1], L);
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) o[k] = 0.f;
-  float lsum = 0.f;
-  float mh = m[0];
-#pragma unroll
-  for (int h = 1; h < QPG; ++h)
-    if (h == hh) mh = m[h];
-  auto pv_rows = [&](const uint8_t *rows, const uint16_t *grow, int a, int e) {
-    int j = a + ((qs - a % NQS) % NQS + NQS) % NQS;
-    for (; j < e; j += NQS) {
-      const float pj = __expf(s_buf[hh * CH + j] - mh);
-      lsum += pj;
-      if constexpr (DPL == 2) {
-        uint32_t w;
-        if (rows) w = *reinterpret_cast<const uint32_t *>(rows + (size_t)(j - a) * D * 2 + lane * 4);
-        else w = __ldcg(reinterpret_cast<const unsigned int *>(grow + lane * 2));
-        o[0] = fmaf(pj, bf_lo(w), o[0]);
-        o[1] = fmaf(pj, bf_hi(w), o[1]);
-      } else {
-        uint2 w;
-        if (rows) w = *reinterpret_cast<const uint2 *>(rows + (size_t)(j - a) * D * 2 + lane * 8);
-        else w = __ldcg(reinterpret_cast<const uint2 *>(grow + lane * 4));
-        o[0] = fmaf(pj, bf_lo(w.x), o[0]);
-        o[1] = fmaf(pj, bf_hi(w.x), o[1]);
-        o[2] = fmaf(pj, bf_lo(w.y), o[2]);
-        o[3] = fmaf(pj, bf_hi(w.y), o[3]);
+        for (int k = 0; k < DPL; ++k) acc[k] = fmaf(a, op[w * D + lane * DPL + k], acc[k]);
       }
     }
-  };
-  for (int p = 0; p < npk; ++p) {
-    const uint32_t seq = meta.seq0 + npk + p, slot = seq % E;
-    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
-    const int a = p * rpp, e = min(n_old, a + rpp);
-    pv_rows(S.ring + (size_t)slot * P.page_bytes, nullptr, a, e);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
-  }
-  if (n_tot > n_old) pv_rows(nullptr, P.vc + kv_row(P, in.layer, b, g, pos), n_old, n_tot);
+    const int PS = 2 * QPG + QPG * D;
+    float *dst = P.part + (((size_t)b * P.nkv + g) * P.nchunk + in.chunk) * PS;
 #pragma unroll
-  for (int k = 0; k < DPL; ++k) S.opart[cw * D + lane * DPL + k] = o[k];
-  if (lane == 0) S.lpart[cw] = lsum;
-  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
-  if (cw < QPG) {
-    const int h = cw, nh = (kComputeWarps - 1 - h) / QPG + 1;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) {
-      float acc = 0.f;
-      for (int r = 0; r < nh; ++r) acc += S.opart[(h + r * QPG) * D + lane * DPL + k];
-      res[2 * QPG + h * D + lane * DPL + k] = acc;
-    }
+    for (int k = 0; k < DPL; ++k) dst[2 * QPG + cw * D + lane * DPL + k] = acc[k];
     if (lane == 0) {
-      float l = 0.f, mv = m[0];
-      for (int r = 0; r < nh; ++r) l += S.lpart[h + r * QPG];
-#pragma unroll
-      for (int hq = 1; hq < QPG; ++hq)
-        if (hq == h) mv = m[hq];
-      res[h] = mv;
-      res[QPG + h] = l;
+      dst[cw] = M;
+      dst[QPG + cw] = L;
     }
   }
   return true;
 }
 
 DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
-                        const SlotMeta &meta, float *res, int cw, int lane, uint32_t &att_uses) {
+                        const SlotMeta &meta, int cw, int lane, uint32_t &att_uses) {
   if (P.d == 64) {
     switch (P.qpg) {
-      case 1: return attn_chunk<64, 1>(P, S, in, meta, res, cw, lane, att_uses);
-      case 2: return attn_chunk<64, 2>(P, S, in, meta, res, cw, lane, att_uses);
-      case 4: return attn_chunk<64, 4>(P, S, in, meta, res, cw, lane, att_uses);
-      default: return attn_chunk<64, 8>(P, S, in, meta, res, cw, lane, att_uses);
+      case 1: return attn_chunk<64, 1>(P, S, in, meta, cw, lane, att_uses);
+      case 2: return attn_chunk<64, 2>(P, S, in, meta, cw, lane, att_uses);
+      case 4: return attn_chunk<64, 4>(P, S, in, meta, cw, lane, att_uses);
+      default: return attn_chunk<64, 8>(P, S, in, meta, cw, lane, att_uses);
     }
   }
   switch (P.qpg) {
-    case 1: return attn_chunk<128, 1>(P, S, in, meta, res, cw, lane, att_uses);
-    case 2: return attn_chunk<128, 2>(P, S, in, meta, res, cw, lane, att_uses);
-    case 4: return attn_chunk<128, 4>(P, S, in, meta, res, cw, lane, att_uses);
-    default: return attn_chunk<128, 8>(P, S, in, meta, res, cw, lane, att_uses);
+    case 1: return attn_chunk<128, 1>(P, S, in, meta, cw, lane, att_uses);
+    case 2: return attn_chunk<128, 2>(P, S, in, meta, cw, lane, att_uses);
+    case 4: return attn_chunk<128, 4>(P, S, in, meta, cw, lane, att_uses);
+    default: return attn_chunk<128, 8>(P, S, in, meta, cw, lane, att_uses);
   }
 }
 
@@ -924,8 +1036,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
       preload_gain_b1(P, in, cw % ns, lane, X);
     xkey = key;
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return false;
-    if (reload && gain_of(P, in.op, in.layer) != nullptr &&
-        !stage_norm_input(P, S, in, cw, lane, xbar_uses))
+    if (reload && stages_input(P, in) && !stage_input(P, S, in, cw, lane, xbar_uses))
       return false;
     if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, reload))
       return false;
@@ -957,7 +1068,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
     float *res = S.res + (size_t)f * P.res_floats;
     bool ok;
     if (in.op == MK_OP_ATTN) {
-      ok = attn_dispatch(P, S, in, meta, res, cw, lane, att_uses);
+      ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses);
       xkey = 0xFFFFFFFFu;
     } else {
       ok = gemv_bn(P, S, in, meta, res, cw, lane, xkey, xbar_uses, key_changes);
@@ -1038,12 +1149,8 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
       }
       break;
     }
-    case MK_OP_ATTN: {
-      const int qpg = P.qpg, PS = 2 * qpg + qpg * d;
-      float *dst = P.part + (((size_t)in.b * P.nkv + in.g) * P.nchunk + in.chunk) * PS;
-      for (int k = lane; k < PS; k += 32) dst[k] = res[k];
-      break;
-    }
+    case MK_OP_ATTN:
+      break;  // the compute warps wrote the chunk partial to global memory
   }
   fence_gpu();
   __syncwarp();
@@ -1055,44 +1162,46 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
     __syncwarp();
     old = __shfl_sync(0xFFFFFFFFu, old, 0);
     if (old == epoch * in.nchunk + in.nchunk - 1u) {
-      // last chunk of (b, g): merge the chunk partials by log-sum-exp; each
-      // lane owns 8 consecutive outputs and loads four chunks at a time
+      // last chunk of (b, g): merge the chunk partials by log-sum-exp.  Each
+      // lane owns 4 consecutive outputs of one head per pass and keeps eight
+      // chunks' loads in flight at a time.
       const int qpg = P.qpg, PS = 2 * qpg + qpg * d, nout = qpg * d;
       const float *pb = P.part + ((size_t)in.b * P.nkv + in.g) * P.nchunk * PS;
-      for (int o0 = lane * 8; o0 < nout; o0 += 256) {
-        const int h = o0 / d, dim0 = o0 % d;
-        float M = -INFINITY, den = 0.f, num[8];
+      for (int o0 = lane * 4; o0 < nout; o0 += 128) {
+        const int h = o0 / d;
+        float M = -INFINITY, den = 0.f;
+        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint32_t c0 = 0; c0 < in.nchunk; c0 += 8) {
+          float mc[8], lc[8];
+          float4 oc[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) num[k] = 0.f;
-        for (uint32_t c0 = 0; c0 < in.nchunk; c0 += 4) {
-          float mc[4], lc[4], oc[4][8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
             mc[u] = -INFINITY;
             lc[u] = 0.f;
+            oc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c0 + u < in.nchunk) {
               const float *pc = pb + (size_t)(c0 + u) * PS;
               mc[u] = __ldcg(pc + h);
               lc[u] = __ldcg(pc + qpg + h);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) oc[u][k] = __ldcg(pc + 2 * qpg + h * d + dim0 + k);
+              oc[u] = __ldcg(reinterpret_cast<const float4 *>(pc + 2 * qpg + o0));
             }
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 8; ++u) {
             if (mc[u] == -INFINITY) continue;
             const float Mn = fmaxf(M, mc[u]);
             const float a = __expf(M - Mn), w = __expf(mc[u] - Mn);
             den = den * a + w * lc[u];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) num[k] = num[k] * a + w * oc[u][k];
+            num.x = num.x * a + w * oc[u].x;
+            num.y = num.y * a + w * oc[u].y;
+            num.z = num.z * a + w * oc[u].z;
+            num.w = num.w * a + w * oc[u].w;
             M = Mn;
           }
         }
-        float *out = P.attn + (size_t)in.b * P.nq * d + ((size_t)in.g * qpg + h) * d + dim0;
         const float inv = 1.f / den;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) out[k] = num[k] * inv;
+        float *out = P.attn + (size_t)in.b * P.nq * d + (size_t)in.g * qpg * d + o0;
+        *reinterpret_cast<float4 *>(out) = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       }
       fence_gpu();
       __syncwarp();
@@ -1156,8 +1265,14 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
 extern "C" __global__ void __launch_bounds__(kThreads, 1)
     mk_megakernel(const __grid_constant__ KParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  const Smem S = make_smem(P, smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The table of shared-memory pointers lives in shared memory itself: a
+  // per-thread copy would sit in local memory, which the small L1 left
+  // beside a full shared-memory carve-out cannot hold for 512 threads.
+  Smem *desc = reinterpret_cast<Smem *>(smem + P.off_misc + kMiscDescOffset);
+  if (tid == 0) *desc = make_smem(P, smem);
+  __syncthreads();
+  const Smem &S = *desc;
   if (tid == 0) {
     for (uint32_t i = 0; i < P.ring_pages; ++i) {
       mbar_init(&S.full[i], 1);

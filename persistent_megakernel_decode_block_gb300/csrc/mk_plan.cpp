@@ -103,14 +103,17 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   auto tile_pages = [&](int op, uint32_t wrows) { return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp); };
 
   // ---- attention chunking ----------------------------------------------
-  uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : 0;
-  if (!ch) {
-    ch = 64;
-    while (ch < 256 && ch * 16 < (uint32_t)c.max_ctx) ch *= 2;
-  }
-  if (ch % 16 || ch < 16 || ch > 1024) REJECT("attn_chunk must be a multiple of 16 in 16..1024");
+  // A chunk holds at most one page of keys and one page of values, so its
+  // instruction streams two pages and indexes rows without division.
+  const uint32_t rpp = page / (2 * (uint32_t)d);  // key (or value) rows per page
+  uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : rpp;
+  if (ch % 16 || ch < 16 || ch > rpp)
+    REJECT("attn_chunk must be a multiple of 16 and at most one page of keys");
   P.attn_chunk = ch;
   P.nchunk = cdiv(c.max_ctx, ch);
+  // each compute warp keeps the scores of its share of a chunk; a head has
+  // at least kComputeWarps / qpg warps
+  P.att_lmax = (uint32_t)align_up(cdiv(ch, (uint32_t)(kComputeWarps / qpg)), 4);
 
   // ---- counters ----------------------------------------------------------
   P.n_wait = (uint32_t)L * (nkv + 4);
@@ -314,8 +317,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   }
 
   // ---- shared-memory layout -------------------------------------------------
-  P.res_floats = (uint32_t)std::max(kMaxItems * B, 2 * qpg + qpg * d);
-  P.res_floats = (P.res_floats + 3) / 4 * 4;
+  P.res_floats = (uint32_t)align_up((uint64_t)kMaxItems * B, 4);
   uint32_t fixed = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
     fixed = (uint32_t)align_up(fixed, align);
@@ -327,15 +329,19 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_fifo = take(kFifo * 64, 64);
   uint32_t rel_meta = take(kFifo * sizeof(SlotMeta), 16);
   uint32_t rel_res = take(kFifo * P.res_floats * 4, 16);
-  uint32_t att_bytes = (qpg * ch + kComputeWarps * d + kComputeWarps) * 4;
+  // attention: per-warp partials {o[d]} and {m, l}, double-buffered, then
+  // per-warp scores
+  uint32_t att_bytes = (2 * kComputeWarps * d + 2 * kComputeWarps * 2 + kComputeWarps * P.att_lmax) * 4;
   uint32_t rel_att = take(att_bytes, 16);
   uint32_t rel_sat = take(P.n_wait * 4, 16);
   uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
   uint32_t rel_rope = take(B * d * 4, 16);
   uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
-  uint32_t rel_misc = take(64, 16);
+  uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
   uint32_t rel_rbuf = take(kMaxItems * kMaxBatch * 4, 16);  // storer's prefetched residuals
-  uint32_t rel_xs = take((H + kComputeWarps) * 4, 16);        // staged normalised input
+  // staged GEMV input (normalised x, or the attention output) and attention scores
+  const uint32_t xs_floats = std::max<uint32_t>(H, QD);
+  uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
   uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 2) * 8;
   uint32_t rel_bars = take(bars_max, 8);
   uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;

@@ -24,7 +24,7 @@ struct HostPlan {
   uint64_t off_lm = 0, off_norms = 0, off_embed = 0, arena_bytes = 0, weight_bytes = 0;
   bool embed_alias = false;  // embedding rows read from the LM-head block
   uint32_t n_wait = 0, n_ctr = 0, lm_ctr = 0;
-  uint32_t attn_chunk = 0, nchunk = 0;
+  uint32_t attn_chunk = 0, nchunk = 0, att_lmax = 0;
   // shared-memory layout
   uint32_t ring_pages = 0, page_bytes = 0, res_floats = 0;
   uint32_t off_bars = 0, off_fifo = 0, off_meta = 0, off_res = 0, off_att = 0, off_sat = 0,

@@ -190,16 +190,25 @@ static int setup_device(mk_plan_s *p) {
   P.qpg = c.n_q_heads / c.n_kv_heads;
   P.nchunk = (int32_t)H.nchunk;
   P.attn_chunk = (int32_t)H.attn_chunk;
+  P.att_lmax = (int32_t)H.att_lmax;
   P.eps = c.rms_eps;
   P.attn_scale = (float)(1.0 / sqrt((double)d));
   P.n_wait = (int32_t)H.n_wait;
   P.mode = c.sched_mode == MK_SCHED_STATIC ? kModeStatic : kModeDynamic;
   P.n_blocks = H.num_sms;
   P.flags = c.flags;
-  P.timeout_ns = (uint64_t)(c.wait_timeout_us > 0 ? c.wait_timeout_us : 1000000) * 1000ull;
+  // wait limits count SM cycles; budget them at the maximum SM clock
+  int clk_khz = 2100000;
+  if (cudaDeviceGetAttribute(&clk_khz, cudaDevAttrClockRate, p->device) != cudaSuccess || clk_khz <= 0) {
+    (void)cudaGetLastError();
+    clk_khz = 2100000;
+  }
+  P.timeout_cycles = (uint64_t)(c.wait_timeout_us > 0 ? c.wait_timeout_us : 1000000) * (uint64_t)clk_khz / 1000ull;
   // static lists may run a full FIFO ahead; the dynamic queue claims close
   // to need so the claims still balance the blocks
   P.lookahead = P.mode == kModeStatic ? (uint32_t)kFifo : 3u;
+  P.loader_idle_ns = 64;
+  P.l2_window = c.l2_prefetch_kb > 0 ? (uint32_t)c.l2_prefetch_kb * 1024u : 0u;
   P.ring_pages = H.ring_pages;
   P.page_bytes = H.page_bytes;
   P.off_bars = H.off_bars;

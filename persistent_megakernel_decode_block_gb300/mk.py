@@ -32,7 +32,8 @@ class mk_config(ctypes.Structure):
                                     "ffn_dim", "vocab")] + [
         ("rms_eps", _f32), ("rope_theta", _f32), ("tie_embeddings", _i32), ("batch", _i32),
         ("max_ctx", _i32), ("sched_mode", _i32), ("flags", _u32), ("wait_timeout_us", _i32),
-        ("num_sms", _i32), ("smem_bytes", _i32), ("page_bytes", _i32), ("attn_chunk", _i32)]
+        ("num_sms", _i32), ("smem_bytes", _i32), ("page_bytes", _i32), ("attn_chunk", _i32),
+        ("l2_prefetch_kb", _i32)]
 
 
 class mk_plan_info_t(ctypes.Structure):

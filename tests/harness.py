@@ -118,6 +118,7 @@ def kv_matches_oracle(setup):
             a = synth.bf16_to_f32(gpu).astype(np.float64)
             b = synth.bf16_to_f32(ref).astype(np.float64)
             bad = np.abs(a - b) > 2.0 ** -7 * np.maximum(np.abs(b), 2.0 ** -6)
-            assert not bad.any(), "KV cache differs beyond one rounding step at %s" % (
-                np.argwhere(bad)[:5],)
+            idx = np.argwhere(bad)[:5]
+            assert not bad.any(), "KV cache differs beyond one rounding step at %s: gpu %s oracle %s" % (
+                idx, a[tuple(idx.T)], b[tuple(idx.T)])
     return True
