@@ -12,11 +12,13 @@ namespace mk {
 // storer; the scheduler role is the loader's queue claim).
 constexpr int kComputeWarps = 14;  // 16 warps per block: 4 per SM sub-partition, 128 registers each
 constexpr int kThreads = 32 * (2 + kComputeWarps);
-constexpr int kFifo = 12;       // instructions a block may hold ahead of compute
+constexpr int kFifo = 8;        // instructions a block may hold ahead of compute
 constexpr int kMaxBatch = 16;
 constexpr int kMaxQpg = 8;      // q heads per KV group
-constexpr int kMaxItems = 32;   // work items (row x slice) per GEMV instruction
-constexpr int kMaxChunks = 8;   // 256-column chunks per item (registers per lane / 8)
+constexpr int kMaxItems = 256;  // work items (row x slice) per GEMV instruction
+constexpr int kMaxItemsB = 256; // work items x batch per GEMV instruction
+constexpr int kMaxChunks = 4;   // 256-column chunks per item: the input slice a lane keeps in
+                                // registers (8 per chunk); 4 keeps the GEMV loop free of spills
 constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
 constexpr int kMaxRing = 32;
 // block flags (bail, bad input) at the start of the misc area, then the
@@ -35,7 +37,7 @@ constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2;
 // ipp items are packed per shared-memory page; nch = SW/256 16-byte chunks
 // per lane.
 struct OpGeom {
-  uint32_t K, NS, SW, item_bytes, ipp, nch, rows_per_tile, wrows_per_tile;
+  uint32_t K, NS, SW, item_bytes, ipp, nch;
 };
 
 struct KParams {
@@ -83,8 +85,8 @@ cudaError_t set_megakernel_smem(uint32_t bytes);
 cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
                               cudaStream_t stream);
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream);
-cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map, uint32_t nrows,
-                          const OpGeom &g, uint32_t page, uint64_t tile_stride,
+cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                          const uint64_t *rowtab, uint32_t nrows, const OpGeom &g, uint32_t page,
                           cudaStream_t stream);
 #endif
 

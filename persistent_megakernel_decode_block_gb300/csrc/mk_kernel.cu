@@ -106,6 +106,12 @@ DEVI uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
   return old;
 }
 DEVI void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Release add: every write that happens before it (including other threads'
+// writes ordered before it by a warp or block barrier) is visible to a thread
+// that acquires the counter and sees the increment.
+DEVI void red_release(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // SM cycle counter: cheap to read, used for every wait limit (the limits are
 // budgeted at the maximum SM clock, so a limit is never shorter than stated)
 DEVI uint64_t cycles() { return (uint64_t)clock64(); }
@@ -683,6 +689,22 @@ DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const Slo
     if (stamp && p + 1 == meta.npages) mw.t_pagel = gtimer();
     const uint8_t *page = S.ring + (size_t)slot * P.page_bytes;
     const uint32_t it_end = min(items, (p + 1) * G.ipp);
+    // two items at a time where the page holds both: independent loads and
+    // reductions overlap
+    for (; active && item + A < it_end; item += 2 * A) {
+      const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
+      float a = dot_item_b1(ip, X, G.nch, lane);
+      float c = dot_item_b1(ip + A * G.item_bytes, X, G.nch, lane);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+      }
+      if (lane == 0) {
+        res[item] = a;
+        res[item + A] = c;
+      }
+    }
     for (; active && item < it_end; item += A) {
       const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
       const float acc = warp_sum(dot_item_b1(ip, X, G.nch, lane));
@@ -1081,7 +1103,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
 }
 
 // --------------------------------------------------------------- storer ----
-__device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
+DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
                           const SlotMeta &meta, const float *res, int lane, uint32_t epoch) {
   const int B = P.B, d = P.d;
   const OpGeom &G = P.geom[in.op];
@@ -1093,21 +1115,20 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
   uint32_t *ctr = P.ctr;
   switch (in.op) {
     case MK_OP_QKV: {
-      const int GR = (P.qpg + 2) * d;
-      const int grp = in.row0 / GR, q0 = in.row0 % GR;
-      const int half = d / 2;
-      if (q0 < (P.qpg + 1) * d) {  // q or k rows: rotate pairs
-        const bool is_q = q0 < P.qpg * d;
-        const int head_row0 = is_q ? q0 % d : q0 - P.qpg * d;
-        const int npairs = in.nrows / 2;
-        for (int u = lane; u < npairs * B; u += 32) {
-          const int pr = u % npairs, b = u / npairs;
-          const float x0 = val(2 * pr, b), x1 = val(2 * pr + 1, b);
-          const int i = (head_row0 + 2 * pr) / 2;
+      // rows come in pairs: one RoPE rotation pair (natural dims i and
+      // i + d/2) of a q head or of k, or two consecutive v dims
+      const int GR = (P.qpg + 2) * d, half = d / 2;
+      const int npairs = (int)in.nrows / 2;
+      for (int u = lane; u < npairs * B; u += 32) {
+        const int pr = u % npairs, b = u / npairs;
+        const int R = (int)in.row0 + 2 * pr, grp = R / GR, q = R % GR;
+        const float x0 = val(2 * pr, b), x1 = val(2 * pr + 1, b);
+        if (q < (P.qpg + 1) * d) {
+          const int i = (q % d) / 2;
           const float cs = S.rope[b * d + i], sn = S.rope[b * d + half + i];
           const float o0 = x0 * cs - x1 * sn, o1 = x0 * sn + x1 * cs;
-          if (is_q) {
-            float *qd = P.q + ((size_t)b * P.nq + grp * P.qpg + q0 / d) * d;
+          if (q < P.qpg * d) {
+            float *qd = P.q + ((size_t)b * P.nq + grp * P.qpg + q / d) * d;
             qd[i] = o0;
             qd[i + half] = o1;
           } else {
@@ -1115,12 +1136,10 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
             kd[i] = to_bf(o0);
             kd[i + half] = to_bf(o1);
           }
-        }
-      } else {
-        const int dim0 = q0 - (P.qpg + 1) * d;
-        for (int u = lane; u < (int)in.nrows * B; u += 32) {
-          const int r = u % in.nrows, b = u / in.nrows;
-          P.vc[kv_row(P, in.layer, b, grp, S.pos[b]) + dim0 + r] = to_bf(val(r, b));
+        } else {
+          uint16_t *vd = P.vc + kv_row(P, in.layer, b, grp, S.pos[b]) + (q - (P.qpg + 1) * d);
+          vd[0] = to_bf(x0);
+          vd[1] = to_bf(x1);
         }
       }
       break;
@@ -1152,10 +1171,12 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
     case MK_OP_ATTN:
       break;  // the compute warps wrote the chunk partial to global memory
   }
-  fence_gpu();
+  // the warp barrier orders every lane's output writes before lane 0's
+  // release (the compute warps' chunk partials were ordered before this
+  // warp by the slot's done barrier)
   __syncwarp();
   if (in.op != MK_OP_ATTN) {
-    if (lane == 0) red_add(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+    if (lane == 0) red_release(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
   } else {
     uint32_t old = 0;
     if (lane == 0) old = atom_add_acq_rel(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
@@ -1203,9 +1224,8 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
         float *out = P.attn + (size_t)in.b * P.nq * d + (size_t)in.g * qpg * d + o0;
         *reinterpret_cast<float4 *>(out) = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
       }
-      fence_gpu();
       __syncwarp();
-      if (lane == 0) red_add(ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
+      if (lane == 0) red_release(ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
     }
   }
   if (lane == 0) {
@@ -1231,15 +1251,12 @@ __device__ __noinline__ void storer_epilogue(const KParams &P, const Smem &S, co
 DEVI void prefetch_residual(const KParams &P, const Smem &S, const mk_instr &in, int lane) {
   if (in.op != MK_OP_OPROJ && in.op != MK_OP_DOWN) return;
   const int n = (int)in.nrows * P.B;
-#pragma unroll
-  for (int i = 0; i < kMaxItems * kMaxBatch / 32; ++i) {
-    const int u = lane + 32 * i;
-    if (u < n) {
-      const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
-      S.rbuf[u] = (in.op == MK_OP_OPROJ && (in.flags & 1))
-                      ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
-                      : __ldcg(P.x + (size_t)b * P.H + row);
-    }
+#pragma unroll 4
+  for (int u = lane; u < n; u += 32) {
+    const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
+    S.rbuf[u] = (in.op == MK_OP_OPROJ && (in.flags & 1))
+                    ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
+                    : __ldcg(P.x + (size_t)b * P.H + row);
   }
 }
 
@@ -1337,12 +1354,13 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
 extern "C" __global__ void mk_epoch_advance(uint32_t *ctrl) { ctrl[kCtlEpoch] += 1u; }
 
 // Re-tiling of one weight block: tile-row k of a block whose source row is
-// map[k] (identity when map is NULL) is split into NS items of item_bytes,
-// packed ipp per page of `page` bytes; tiles are tile_stride bytes apart.
+// Arena row k takes source row map[k] (k when map is NULL), split into NS
+// items of item_bytes packed ipp per page; rowtab[k] = byte offset of its
+// tile | its row within the tile (tiles are page-aligned, rows < 4096).
 extern "C" __global__ void mk_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
-                                     uint32_t nrows, uint32_t K, uint32_t NS,
-                                     uint32_t item_bytes, uint32_t ipp, uint32_t page,
-                                     uint32_t wrows_per_tile, uint64_t tile_stride) {
+                                     const uint64_t *rowtab, uint32_t nrows, uint32_t K,
+                                     uint32_t NS, uint32_t item_bytes, uint32_t ipp,
+                                     uint32_t page) {
   const uint64_t per_row = (uint64_t)K * 2 / 16;
   const uint64_t total = (uint64_t)nrows * per_row;
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -1350,9 +1368,10 @@ extern "C" __global__ void mk_retile(uint8_t *dst, const uint8_t *src, const int
     const uint32_t k = (uint32_t)(i / per_row);
     const uint32_t cb = (uint32_t)(i % per_row) * 16;
     const uint32_t s = cb / item_bytes, ib = cb % item_bytes;
-    const uint32_t t = k / wrows_per_tile, r = k % wrows_per_tile;
+    const uint64_t rt = rowtab[k];
+    const uint32_t r = (uint32_t)(rt & 4095u);
     const uint32_t item = r * NS + s;
-    uint8_t *d = dst + t * tile_stride + (uint64_t)(item / ipp) * page +
+    uint8_t *d = dst + (rt & ~(uint64_t)4095u) + (uint64_t)(item / ipp) * page +
                  (uint64_t)(item % ipp) * item_bytes + ib;
     const uint32_t srow = map ? (uint32_t)map[k] : k;
     *reinterpret_cast<uint4 *>(d) =
@@ -1386,14 +1405,13 @@ cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map, uint32_t nrows,
-                          const OpGeom &g, uint32_t page, uint64_t tile_stride,
+cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                          const uint64_t *rowtab, uint32_t nrows, const OpGeom &g, uint32_t page,
                           cudaStream_t stream) {
   const uint64_t total = (uint64_t)nrows * g.K * 2 / 16;
   const uint32_t blocks = (uint32_t)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
-  mk_retile<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, nrows, g.K, g.NS,
-                                                      g.item_bytes, g.ipp, page,
-                                                      g.wrows_per_tile, tile_stride);
+  mk_retile<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, rowtab, nrows, g.K, g.NS,
+                                                      g.item_bytes, g.ipp, page);
   return cudaGetLastError();
 }
 

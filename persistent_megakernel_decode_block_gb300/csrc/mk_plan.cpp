@@ -19,7 +19,7 @@
 namespace mk {
 
 static void geom_for(uint32_t K, uint32_t page, OpGeom &g) {
-  uint32_t NS = (K + 2047) / 2048;
+  uint32_t NS = (K + 256 * kMaxChunks - 1) / (256 * kMaxChunks);
   while (K % (NS * 256)) NS++;
   g.K = K;
   g.NS = NS;
@@ -68,39 +68,77 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
             F = c.ffn_dim, V = c.vocab, B = c.batch;
   const int qpg = nq / nkv, GR = (qpg + 2) * d, QD = nq * d;
 
-  // ---- GEMV geometry and tile sizes ------------------------------------
+  // ---- GEMV geometry and tiles -------------------------------------------
+  // Each phase is cut into a multiple of the SM count of tiles whose sizes
+  // differ by at most one unit, so the static round-robin lists hand every
+  // block the same share of every phase (one tile per block and phase where
+  // the item limit allows).  Units: rotation pairs for q/k/v rows (a pair is
+  // one RoPE rotation); whole pages of rows for a tied LM head (its tiles
+  // then are the plain embedding matrix); single outputs otherwise.
   geom_for(H, page, P.geom[MK_OP_QKV]);
   geom_for(QD, page, P.geom[MK_OP_OPROJ]);
   geom_for(H, page, P.geom[MK_OP_GATEUP]);
   geom_for(F, page, P.geom[MK_OP_DOWN]);
   geom_for(H, page, P.geom[MK_OP_LMHEAD]);
-  auto rows_for = [&](int op, uint64_t target_bytes, uint32_t wrows_per_out) {
-    OpGeom &g = P.geom[op];
-    uint32_t cap = kMaxItems / (g.NS * wrows_per_out);
-    uint64_t want = target_bytes / ((uint64_t)2 * g.K * wrows_per_out);
-    uint32_t r = (uint32_t)std::max<uint64_t>(1, std::min<uint64_t>(cap, want));
-    return std::max<uint32_t>(1, r);
-  };
-  {
-    uint32_t r = rows_for(MK_OP_QKV, 65536, 1);
-    r = std::max<uint32_t>(2, r - r % 2);
-    while (d % r) r -= 2;  // a tile never straddles a head; pairs stay whole
-    P.geom[MK_OP_QKV].rows_per_tile = r;
-    P.geom[MK_OP_QKV].wrows_per_tile = r;
-  }
-  P.geom[MK_OP_OPROJ].rows_per_tile = P.geom[MK_OP_OPROJ].wrows_per_tile = rows_for(MK_OP_OPROJ, 65536, 1);
-  P.geom[MK_OP_GATEUP].rows_per_tile = rows_for(MK_OP_GATEUP, 131072, 2);
-  P.geom[MK_OP_GATEUP].wrows_per_tile = 2 * P.geom[MK_OP_GATEUP].rows_per_tile;
-  P.geom[MK_OP_DOWN].rows_per_tile = P.geom[MK_OP_DOWN].wrows_per_tile = rows_for(MK_OP_DOWN, 131072, 1);
-  P.geom[MK_OP_LMHEAD].rows_per_tile = P.geom[MK_OP_LMHEAD].wrows_per_tile = rows_for(MK_OP_LMHEAD, 131072, 1);
   for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
     if (op == MK_OP_ATTN) continue;
     const OpGeom &g = P.geom[op];
     if (g.ipp < 1 || g.nch > (uint32_t)kMaxChunks || g.NS > (uint32_t)kComputeWarps)
       REJECT("GEMV geometry does not fit the compute warps");
-    if (g.wrows_per_tile * g.NS > (uint32_t)kMaxItems) REJECT("tile has too many items");
   }
+  const uint32_t max_items = std::min<uint32_t>(kMaxItems, std::max<uint32_t>(8, kMaxItemsB / B));
+  bool too_big = false;
+  auto split = [&](uint32_t n_out, uint32_t unit, uint32_t step, uint32_t items_per_out) {
+    const uint32_t units = cdiv(n_out, unit);
+    uint32_t t = std::min(step, units);
+    while (t < units && (uint64_t)cdiv(units, t) * unit * items_per_out > max_items)
+      t = std::min(t + step, units);
+    std::vector<uint32_t> sz(t);
+    uint32_t left = n_out;
+    for (uint32_t i = 0; i < t; ++i) {
+      const uint32_t u = units / t + (i < units % t ? 1u : 0u);
+      sz[i] = std::min(u * unit, left);
+      left -= sz[i];
+      if ((uint64_t)sz[i] * items_per_out > max_items) too_big = true;
+    }
+    return sz;
+  };
+  const uint32_t S_ = num_sms;
+  const uint32_t lm_unit = [&] {
+    const OpGeom &g = P.geom[MK_OP_LMHEAD];
+    if (!c.tie_embeddings || page % g.item_bytes) return 1u;
+    uint32_t a = g.ipp, b2 = g.NS;
+    while (b2) { const uint32_t t = a % b2; a = b2; b2 = t; }
+    return g.ipp / a;  // rows per unit: a multiple of whole pages
+  }();
+  P.tiles[MK_OP_QKV] = split(GR, 2, std::max<uint32_t>(1, S_ / nkv), P.geom[MK_OP_QKV].NS);
+  P.tiles[MK_OP_OPROJ] = split(H, 1, S_, P.geom[MK_OP_OPROJ].NS);
+  P.tiles[MK_OP_GATEUP] = split(F, 1, S_, 2 * P.geom[MK_OP_GATEUP].NS);
+  P.tiles[MK_OP_DOWN] = split(H, 1, S_, P.geom[MK_OP_DOWN].NS);
+  P.tiles[MK_OP_LMHEAD] = split(V, lm_unit, S_, P.geom[MK_OP_LMHEAD].NS);
+  if (too_big) REJECT("a GEMV tile has too many items");
+  auto wrows_of = [](int op, uint32_t n) { return op == MK_OP_GATEUP ? 2 * n : n; };
   auto tile_pages = [&](int op, uint32_t wrows) { return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp); };
+  uint32_t tile_items_max = 0;
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
+    for (uint32_t n : P.tiles[op])
+      tile_items_max = std::max(tile_items_max, wrows_of(op, n) * P.geom[op].NS);
+  // arena row k of one layer's block of an op -> byte offset of its tile
+  // (relative to the block) | its row within the tile (below 4096)
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
+    if (op == MK_OP_ATTN) continue;
+    std::vector<uint64_t> &rt = P.rowtab[op];
+    rt.clear();
+    uint64_t toff = 0;
+    const int reps = op == MK_OP_QKV ? nkv : 1;
+    for (int g = 0; g < reps; ++g)
+      for (uint32_t n : P.tiles[op]) {
+        const uint32_t w = wrows_of(op, n);
+        for (uint32_t r = 0; r < w; ++r) rt.push_back(toff | r);
+        toff += (uint64_t)tile_pages(op, w) * page;
+      }
+    P.block_bytes[op] = toff;
+  }
 
   // ---- attention chunking ----------------------------------------------
   // A chunk holds at most one page of keys and one page of values, so its
@@ -128,7 +166,11 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   off = align_up(off + (uint64_t)(2 * L + 1) * H * 2, 4096);
   {
     const OpGeom &g = P.geom[MK_OP_LMHEAD];
-    bool plain = (page % g.item_bytes == 0) && ((g.wrows_per_tile * g.NS) % g.ipp == 0);
+    // plain: every tile but the last fills whole pages, so the LM-head block
+    // is the row-major embedding matrix itself
+    bool plain = page % g.item_bytes == 0;
+    const std::vector<uint32_t> &t = P.tiles[MK_OP_LMHEAD];
+    for (size_t i = 0; i + 1 < t.size(); ++i) plain = plain && (t[i] * g.NS) % g.ipp == 0;
     P.embed_alias = c.tie_embeddings && plain;
   }
   if (!P.embed_alias) {
@@ -156,35 +198,31 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     in.sig2_ctr = MK_NO_COUNTER;
     return in;
   };
-  const uint32_t nO = cdiv(H, P.geom[MK_OP_OPROJ].rows_per_tile);
-  const uint32_t nGU = cdiv(F, P.geom[MK_OP_GATEUP].rows_per_tile);
-  const uint32_t nD = cdiv(H, P.geom[MK_OP_DOWN].rows_per_tile);
-  const uint32_t nLM = cdiv(V, P.geom[MK_OP_LMHEAD].rows_per_tile);
-  const uint32_t qkv_r = P.geom[MK_OP_QKV].rows_per_tile, qkv_tiles_per_group = GR / qkv_r;
+  const uint32_t nO = (uint32_t)P.tiles[MK_OP_OPROJ].size();
+  const uint32_t nGU = (uint32_t)P.tiles[MK_OP_GATEUP].size();
+  const uint32_t nD = (uint32_t)P.tiles[MK_OP_DOWN].size();
+  const uint32_t qkv_tiles_per_group = (uint32_t)P.tiles[MK_OP_QKV].size();
   P.off_qkv.resize(L);
   P.off_o.resize(L);
   P.off_gu.resize(L);
   P.off_d.resize(L);
 
-  auto gemv_tiles = [&](uint8_t op, int l, uint32_t nout, uint32_t ntiles, mk_instr proto) {
+  auto gemv_tiles = [&](uint8_t op, mk_instr proto) {
     const OpGeom &g = P.geom[op];
-    const uint32_t full_pages = tile_pages(op, g.wrows_per_tile);
-    for (uint32_t t = 0; t < ntiles; ++t) {
+    uint32_t row0 = 0;
+    for (uint32_t n : P.tiles[op]) {
       mk_instr in = proto;
-      in.row0 = t * g.rows_per_tile;
-      in.nrows = std::min<uint32_t>(g.rows_per_tile, nout - in.row0);
-      uint32_t wrows = op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+      in.row0 = row0;
+      in.nrows = n;
+      const uint32_t wrows = wrows_of(op, n);
       in.npages = tile_pages(op, wrows);
-      in.wofs = off + (uint64_t)t * full_pages * page;
+      in.wofs = off;
+      off += (uint64_t)in.npages * page;
+      row0 += n;
       P.weight_bytes += (uint64_t)wrows * g.K * 2;
       push(in);
       P.ctr_inc[in.sig_ctr]++;
     }
-    off += (uint64_t)(ntiles - 1) * full_pages * page +
-           (uint64_t)tile_pages(op, op == MK_OP_GATEUP
-                                        ? 2 * (nout - (ntiles - 1) * g.rows_per_tile)
-                                        : nout - (ntiles - 1) * g.rows_per_tile) * page;
-    off = align_up(off, page);
   };
 
   for (int l = 0; l < L; ++l) {
@@ -193,9 +231,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     P.off_qkv[l] = off;
     {
       const OpGeom &g = P.geom[MK_OP_QKV];
-      const uint32_t tp = tile_pages(MK_OP_QKV, qkv_r);
-      for (int grp = 0; grp < nkv; ++grp)
-        for (uint32_t t = 0; t < qkv_tiles_per_group; ++t) {
+      for (int grp = 0; grp < nkv; ++grp) {
+        uint32_t r0 = 0;
+        for (uint32_t n : P.tiles[MK_OP_QKV]) {
           mk_instr in = base(MK_OP_QKV, l);
           in.flags = l == 0 ? 1 : 0;
           in.g = (uint16_t)grp;
@@ -204,15 +242,17 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
             in.wait_tgt = nD;
           }
           in.sig_ctr = ctr_qkv(c, l, grp);
-          in.row0 = grp * GR + t * qkv_r;
-          in.nrows = qkv_r;
-          in.npages = tp;
+          in.row0 = grp * GR + r0;
+          in.nrows = n;
+          in.npages = tile_pages(MK_OP_QKV, n);
           in.wofs = off;
-          off += (uint64_t)tp * page;
-          P.weight_bytes += (uint64_t)qkv_r * g.K * 2;
+          off += (uint64_t)in.npages * page;
+          r0 += n;
+          P.weight_bytes += (uint64_t)n * g.K * 2;
           push(in);
           P.ctr_inc[in.sig_ctr]++;
         }
+      }
     }
     // attention chunks, group-major
     new_phase(MK_OP_ATTN, l);
@@ -242,7 +282,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       in.wait_ctr = ctr_attn(c, l);
       in.wait_tgt = (uint32_t)B * nkv;
       in.sig_ctr = ctr_o(c, l);
-      gemv_tiles(MK_OP_OPROJ, l, H, nO, in);
+      gemv_tiles(MK_OP_OPROJ, in);
     }
     // RMSNorm + gate/up + SiLU*mul
     new_phase(MK_OP_GATEUP, l);
@@ -252,7 +292,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       in.wait_ctr = ctr_o(c, l);
       in.wait_tgt = nO;
       in.sig_ctr = ctr_gu(c, l);
-      gemv_tiles(MK_OP_GATEUP, l, F, nGU, in);
+      gemv_tiles(MK_OP_GATEUP, in);
     }
     // down-projection + residual
     new_phase(MK_OP_DOWN, l);
@@ -262,7 +302,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       in.wait_ctr = ctr_gu(c, l);
       in.wait_tgt = nGU;
       in.sig_ctr = ctr_d(c, l);
-      gemv_tiles(MK_OP_DOWN, l, H, nD, in);
+      gemv_tiles(MK_OP_DOWN, in);
     }
   }
   new_phase(MK_OP_LMHEAD, 0);
@@ -272,7 +312,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     in.wait_ctr = ctr_d(c, L - 1);
     in.wait_tgt = nD;
     in.sig_ctr = P.lm_ctr;
-    gemv_tiles(MK_OP_LMHEAD, 0, V, nLM, in);
+    gemv_tiles(MK_OP_LMHEAD, in);
   }
   P.arena_bytes = align_up(off, 4096);
 
@@ -306,18 +346,19 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     P.qkv_map[R] = nat;
   }
   {
-    const uint32_t r = P.geom[MK_OP_GATEUP].rows_per_tile;
     P.gu_map.resize((size_t)2 * F);
     size_t k = 0;
-    for (uint32_t t = 0; t < nGU; ++t) {
-      uint32_t r0 = t * r, nr = std::min<uint32_t>(r, F - r0);
+    uint32_t r0 = 0;
+    for (uint32_t nr : P.tiles[MK_OP_GATEUP]) {
       for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(r0 + j);
       for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(F + r0 + j);
+      r0 += nr;
     }
   }
 
   // ---- shared-memory layout -------------------------------------------------
-  P.res_floats = (uint32_t)align_up((uint64_t)kMaxItems * B, 4);
+  // per-slot dot products (items x batch); also the size of the storer's residual buffer
+  P.res_floats = (uint32_t)align_up((uint64_t)tile_items_max * B, 4);
   uint32_t fixed = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
     fixed = (uint32_t)align_up(fixed, align);
@@ -338,7 +379,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_rope = take(B * d * 4, 16);
   uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
   uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
-  uint32_t rel_rbuf = take(kMaxItems * kMaxBatch * 4, 16);  // storer's prefetched residuals
+  uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
   // staged GEMV input (normalised x, or the attention output) and attention scores
   const uint32_t xs_floats = std::max<uint32_t>(H, QD);
   uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);

@@ -19,6 +19,9 @@ struct HostPlan {
   std::vector<int32_t> qkv_map;  // permuted q/k/v row -> row of [Wq; Wk; Wv]
   std::vector<int32_t> gu_map;   // gate/up tile row -> row of [Wg; Wu]
   OpGeom geom[8]{};
+  std::vector<uint32_t> tiles[8];    // per op: outputs of each tile (QKV: of one group)
+  std::vector<uint64_t> rowtab[8];   // per op: arena row -> tile byte offset | row in tile
+  uint64_t block_bytes[8]{};         // per op: arena bytes of one layer's block
   // weight arena (bytes)
   std::vector<uint64_t> off_qkv, off_o, off_gu, off_d;
   uint64_t off_lm = 0, off_norms = 0, off_embed = 0, arena_bytes = 0, weight_bytes = 0;

@@ -335,11 +335,6 @@ static int copy_in(void *dst, const void *src, size_t bytes, cudaStream_t s) {
   return MK_OK;
 }
 
-static uint64_t tile_stride(const HostPlan &H, int op) {
-  const OpGeom &g = H.geom[op];
-  return (uint64_t)((g.wrows_per_tile * g.NS + g.ipp - 1) / g.ipp) * H.page_bytes;
-}
-
 MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
   if (!p || !w || !w->embed || !w->final_norm || !w->layers) return MK_ERR_ARG;
   if (p->host_only) return MK_ERR_STATE;
@@ -362,12 +357,31 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
   stage_elems = std::max(stage_elems, V * H_);
   uint8_t *stage = nullptr;
   if (dalloc(&stage, stage_elems * 2) != MK_OK) return MK_ERR_NOMEM;
+  // the planner's row tables (arena row -> tile offset | row in tile), one per op
+  size_t rt_rows = 0, rt_at[8] = {};
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
+    rt_at[op] = rt_rows;
+    rt_rows += H.rowtab[op].size();
+  }
+  uint64_t *rowtab = nullptr;
+  if (dalloc(&rowtab, rt_rows) != MK_OK) {
+    cudaFree(stage);
+    return MK_ERR_NOMEM;
+  }
   int rc = MK_OK;
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD && rc == MK_OK; ++op)
+    if (!H.rowtab[op].empty() &&
+        cudaMemcpy(rowtab + rt_at[op], H.rowtab[op].data(), H.rowtab[op].size() * 8,
+                   cudaMemcpyHostToDevice) != cudaSuccess) {
+      (void)cudaGetLastError();
+      rc = MK_ERR_CUDA;
+    }
   const uint32_t pg = H.page_bytes;
   uint8_t *A = p->d_arena;
   auto norm_dst = [&](int idx) { return A + H.off_norms + (size_t)idx * H_ * 2; };
   auto retile = [&](uint8_t *dst, const int32_t *map, uint32_t rows, int op) {
-    cudaError_t e = launch_retile(dst, stage, map, rows, H.geom[op], pg, tile_stride(H, op), s);
+    if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
+    cudaError_t e = launch_retile(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], pg, s);
     return e == cudaSuccess ? MK_OK : cuda_code(e);
   };
 #define TRY(x)                  \
@@ -375,6 +389,7 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
     (void)cudaGetLastError();   \
     goto done;                  \
   }
+  TRY(rc);
   for (int l = 0; l < c.n_layers; ++l) {
     const mk_layer_weights &lw = w->layers[l];
     TRY(copy_in(norm_dst(2 * l), lw.attn_norm, H_ * 2, s));
@@ -403,6 +418,7 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
 done:
   cudaStreamSynchronize(s);
   cudaFree(stage);
+  cudaFree(rowtab);
   if (rc == MK_OK) p->weights_loaded = true;
   return rc;
 }
