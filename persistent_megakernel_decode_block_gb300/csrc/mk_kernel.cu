@@ -842,27 +842,32 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   }
   if (stamp) mw.t_input = gtimer();
   const bool paged = n_old > 0;  // one key page and one value page
-  const uint8_t *kpage = S.ring + (size_t)(meta.seq0 % E) * P.page_bytes;
-  const uint8_t *vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
+  const uint8_t *__restrict__ kpage = S.ring + (size_t)(meta.seq0 % E) * P.page_bytes;
+  const uint8_t *__restrict__ vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
   if (paged && !warp_wait(P, S, &S.full[meta.seq0 % E], (meta.seq0 / E) & 1u, kWhereCompute | meta.idx))
     return false;
   if (stamp) mw.t_page0 = gtimer();
 
-  // 1. scores of rows j0..j1 into this warp's row of S.sc
-  float *sw = S.sc + (size_t)cw * P.att_lmax;
-#pragma unroll 2
-  for (int jb = j0; jb < j1; jb += RPS) {
-    const int j = jb + lane / LPP;
-    float dsum = 0.f;
-    if (j < j1) {
+  // 1. scores of rows j0..j1 into this warp's row of S.sc.  A block of LPP
+  //    steps covers 32 rows; each lane keeps its LPP partial dot products and
+  //    one transposing butterfly over the LPP lanes of a row group leaves
+  //    lane `part` with the full score of step `part` (LPP - 1 shuffles for
+  //    LPP rows instead of log2(LPP) per row).
+  float *__restrict__ sw = S.sc + (size_t)cw * P.att_lmax;
+  for (int jb = j0; jb < j1; jb += LPP * RPS) {
+    float v[LPP];
+#pragma unroll
+    for (int t = 0; t < LPP; ++t) {
+      const int j = jb + t * RPS + lane / LPP;
       float k8[8];
       if (j < n_old) {
         const uint4 w = *reinterpret_cast<const uint4 *>(kpage + (size_t)j * D * 2 + part * 16);
         k8[0] = bf_lo(w.x); k8[1] = bf_hi(w.x); k8[2] = bf_lo(w.y); k8[3] = bf_hi(w.y);
         k8[4] = bf_lo(w.z); k8[5] = bf_hi(w.z); k8[6] = bf_lo(w.w); k8[7] = bf_hi(w.w);
       } else {
+        const bool cur = j < j1;  // the row of p_b itself
 #pragma unroll
-        for (int u = 0; u < 8; ++u) k8[u] = kn8[u];
+        for (int u = 0; u < 8; ++u) k8[u] = cur ? kn8[u] : 0.f;
       }
       float a0 = 0.f, a1 = 0.f;
 #pragma unroll
@@ -870,11 +875,20 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
         a0 = fmaf(q8[u], k8[u], a0);
         a1 = fmaf(q8[u + 1], k8[u + 1], a1);
       }
-      dsum = a0 + a1;
+      v[t] = a0 + a1;
     }
 #pragma unroll
-    for (int o = LPP / 2; o; o >>= 1) dsum += __shfl_xor_sync(0xFFFFFFFFu, dsum, o);
-    if (part == 0 && j < j1) sw[j - j0] = dsum;
+    for (int hw = LPP / 2; hw >= 1; hw /= 2) {
+      const bool upper = (part & hw) != 0;
+#pragma unroll
+      for (int i = 0; i < hw; ++i) {
+        const float send = upper ? v[i] : v[i + hw];
+        const float keep = upper ? v[i + hw] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, hw);
+      }
+    }
+    const int jr = jb + part * RPS + lane / LPP;
+    if (jr < j1) sw[jr - j0] = v[0];
   }
   __syncwarp();
 
@@ -896,29 +910,34 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   if (paged && !warp_wait(P, S, &S.full[(meta.seq0 + 1) % E], ((meta.seq0 + 1) / E) & 1u,
                           kWhereCompute | meta.idx))
     return false;
-  float o[4][DPL];
+  float o[8][DPL];
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < 8; ++u)
 #pragma unroll
     for (int k = 0; k < DPL; ++k) o[u][k] = 0.f;
   const int jo = min(j1, n_old);  // rows of this warp that come from the value page
-  const uint8_t *vrow = vpage + lane * DPL * 2;
+  const uint8_t *__restrict__ vrow = vpage + lane * DPL * 2;
   int j = j0;
-  for (; j + 4 <= jo; j += 4) {
+  // eight positions per iteration: two 16-byte loads of probabilities (the
+  // warp's score row is 16-byte aligned and j - j0 steps by 8) and eight
+  // independent accumulators
+  for (; j + 8 <= jo; j += 8) {
+    const float4 pa = *reinterpret_cast<const float4 *>(sw + (j - j0));
+    const float4 pb = *reinterpret_cast<const float4 *>(sw + (j - j0) + 4);
+    const float pj[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float pj = sw[j + u - j0];
+    for (int u = 0; u < 8; ++u) {
       const uint8_t *row = vrow + (size_t)(j + u) * D * 2;
       if constexpr (DPL == 2) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(row);
-        o[u][0] = fmaf(pj, bf_lo(w), o[u][0]);
-        o[u][1] = fmaf(pj, bf_hi(w), o[u][1]);
+        o[u][0] = fmaf(pj[u], bf_lo(w), o[u][0]);
+        o[u][1] = fmaf(pj[u], bf_hi(w), o[u][1]);
       } else {
         const uint2 w = *reinterpret_cast<const uint2 *>(row);
-        o[u][0] = fmaf(pj, bf_lo(w.x), o[u][0]);
-        o[u][1] = fmaf(pj, bf_hi(w.x), o[u][1]);
-        o[u][DPL > 2 ? 2 : 0] = fmaf(pj, bf_lo(w.y), o[u][DPL > 2 ? 2 : 0]);
-        o[u][DPL > 2 ? 3 : 1] = fmaf(pj, bf_hi(w.y), o[u][DPL > 2 ? 3 : 1]);
+        o[u][0] = fmaf(pj[u], bf_lo(w.x), o[u][0]);
+        o[u][1] = fmaf(pj[u], bf_hi(w.x), o[u][1]);
+        o[u][DPL > 2 ? 2 : 0] = fmaf(pj[u], bf_lo(w.y), o[u][DPL > 2 ? 2 : 0]);
+        o[u][DPL > 2 ? 3 : 1] = fmaf(pj[u], bf_hi(w.y), o[u][DPL > 2 ? 3 : 1]);
       }
     }
   }
@@ -952,7 +971,8 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   float *mlp = S.ml + par * kComputeWarps * 2;
 #pragma unroll
   for (int k = 0; k < DPL; ++k)
-    op[cw * D + lane * DPL + k] = (o[0][k] + o[1][k]) + (o[2][k] + o[3][k]);
+    op[cw * D + lane * DPL + k] =
+        ((o[0][k] + o[1][k]) + (o[2][k] + o[3][k])) + ((o[4][k] + o[5][k]) + (o[6][k] + o[7][k]));
   if (lane == 0) {
     mlp[cw * 2] = m;
     mlp[cw * 2 + 1] = l;
