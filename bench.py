@@ -57,6 +57,39 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def kernel_sha256():
+    """Hash of the kernel sources (names and bytes), to tell whether a
+    recorded ncu traffic figure still describes the kernel being timed."""
+    import glob
+    import hashlib
+    pat = os.path.join(ROOT, "persistent_megakernel_decode_block_gb300", "csrc", "*")
+    fs = sorted([f for f in glob.glob(pat) if f.endswith((".cu", ".cpp", ".h"))] +
+                [os.path.join(ROOT, "include", "mk.h")], key=os.path.basename)
+    h = hashlib.sha256()
+    for f in fs:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """dram bytes read + written per launch from the committed ncu summary of
+    this workload, or None when the kernel changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "mk_megakernel_%s_sections.md" % workload)
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line and not line.startswith(("|", "#", " ", "`")):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_sha256():
+            return None
+        return float(kv["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def algorithmic_bytes(m, weight_bytes, positions):
     """weights once + KV rows below each position read + one K/V row written"""
     row = m["n_kv_heads"] * m["head_dim"] * 2  # bytes of one position, one layer, K or V
@@ -319,7 +352,7 @@ def run_mine(a):
         "us_per_token": {"median": 1000 * ms_med, "p10": 1000 * per_sorted[len(per) // 10],
                          "p90": 1000 * per_sorted[(9 * len(per)) // 10]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": recorded_traffic(name),
                      "bytes_per_step": bytes_step, "peak_kind": peak_kind + " hbm_gbs"},
         "gpu_launches": a.steps,
         "e2e": e2e,
