@@ -799,7 +799,7 @@ __device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_i
 template <int D, int QPG>
 __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const mk_instr &in,
                                         const SlotMeta &meta, int cw, int lane,
-                                        uint32_t &att_uses) {
+                                        uint32_t &att_uses, uint32_t epoch) {
   constexpr int LPP = D / 8;      // lanes per key row (16 bytes each)
   constexpr int RPS = 32 / LPP;   // key rows per warp step
   constexpr int DPL = D / 32;     // value dims per lane
@@ -1005,24 +1005,72 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
       dst[QPG + cw] = L;
     }
   }
+
+  // 6. arrival: the chunk that completes its (sequence, group) merges all of
+  //    the group's chunk partials by log-sum-exp, in chunk order, with every
+  //    compute thread (one output each, eight chunks' loads in flight), and
+  //    releases the group counter.  The acq_rel arrival publishes this chunk's
+  //    partial (ordered before it by the barrier) and, for the last arriver,
+  //    acquires every other chunk's.
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (cw == 0 && lane == 0) {
+    const uint32_t old = atom_add_acq_rel(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+    S.misc[2] = old == epoch * in.nchunk + in.nchunk - 1u ? 1 : 0;
+  }
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (S.misc[2]) {
+    const int PS = 2 * QPG + QPG * D, nch = (int)in.nchunk;
+    const float *pb = P.part + ((size_t)b * P.nkv + g) * nch * PS;
+    for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
+      const int h = o / D;
+      float M = -INFINITY, den = 0.f, num = 0.f;
+      for (int c0 = 0; c0 < nch; c0 += 8) {
+        float mc[8], lc[8], oc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          mc[u] = -INFINITY;
+          lc[u] = oc[u] = 0.f;
+          if (c0 + u < nch) {
+            const float *pc = pb + (size_t)(c0 + u) * PS;
+            mc[u] = __ldcg(pc + h);
+            lc[u] = __ldcg(pc + QPG + h);
+            oc[u] = __ldcg(pc + 2 * QPG + o);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (mc[u] == -INFINITY) continue;
+          const float Mn = fmaxf(M, mc[u]);
+          const float a = __expf(M - Mn), w = __expf(mc[u] - Mn);
+          den = den * a + w * lc[u];
+          num = num * a + w * oc[u];
+          M = Mn;
+        }
+      }
+      P.attn[(size_t)b * P.nq * D + (size_t)g * QPG * D + o] = num / den;
+    }
+    if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+    if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
+  }
   return true;
 }
 
 DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
-                        const SlotMeta &meta, int cw, int lane, uint32_t &att_uses) {
+                        const SlotMeta &meta, int cw, int lane, uint32_t &att_uses,
+                        uint32_t epoch) {
   if (P.d == 64) {
     switch (P.qpg) {
-      case 1: return attn_chunk<64, 1>(P, S, in, meta, cw, lane, att_uses);
-      case 2: return attn_chunk<64, 2>(P, S, in, meta, cw, lane, att_uses);
-      case 4: return attn_chunk<64, 4>(P, S, in, meta, cw, lane, att_uses);
-      default: return attn_chunk<64, 8>(P, S, in, meta, cw, lane, att_uses);
+      case 1: return attn_chunk<64, 1>(P, S, in, meta, cw, lane, att_uses, epoch);
+      case 2: return attn_chunk<64, 2>(P, S, in, meta, cw, lane, att_uses, epoch);
+      case 4: return attn_chunk<64, 4>(P, S, in, meta, cw, lane, att_uses, epoch);
+      default: return attn_chunk<64, 8>(P, S, in, meta, cw, lane, att_uses, epoch);
     }
   }
   switch (P.qpg) {
-    case 1: return attn_chunk<128, 1>(P, S, in, meta, cw, lane, att_uses);
-    case 2: return attn_chunk<128, 2>(P, S, in, meta, cw, lane, att_uses);
-    case 4: return attn_chunk<128, 4>(P, S, in, meta, cw, lane, att_uses);
-    default: return attn_chunk<128, 8>(P, S, in, meta, cw, lane, att_uses);
+    case 1: return attn_chunk<128, 1>(P, S, in, meta, cw, lane, att_uses, epoch);
+    case 2: return attn_chunk<128, 2>(P, S, in, meta, cw, lane, att_uses, epoch);
+    case 4: return attn_chunk<128, 4>(P, S, in, meta, cw, lane, att_uses, epoch);
+    default: return attn_chunk<128, 8>(P, S, in, meta, cw, lane, att_uses, epoch);
   }
 }
 
@@ -1110,7 +1158,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
     float *res = S.res + (size_t)f * P.res_floats;
     bool ok;
     if (in.op == MK_OP_ATTN) {
-      ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses);
+      ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses, epoch);
       xkey = 0xFFFFFFFFu;
     } else {
       ok = gemv_bn(P, S, in, meta, res, cw, lane, xkey, xbar_uses, key_changes);
@@ -1194,60 +1242,9 @@ DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
   // the warp barrier orders every lane's output writes before lane 0's
   // release (the compute warps' chunk partials were ordered before this
   // warp by the slot's done barrier)
+  // (attention chunks signal and merge from the compute warps)
   __syncwarp();
-  if (in.op != MK_OP_ATTN) {
-    if (lane == 0) red_release(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
-  } else {
-    uint32_t old = 0;
-    if (lane == 0) old = atom_add_acq_rel(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
-    __syncwarp();
-    old = __shfl_sync(0xFFFFFFFFu, old, 0);
-    if (old == epoch * in.nchunk + in.nchunk - 1u) {
-      // last chunk of (b, g): merge the chunk partials by log-sum-exp.  Each
-      // lane owns 4 consecutive outputs of one head per pass and keeps eight
-      // chunks' loads in flight at a time.
-      const int qpg = P.qpg, PS = 2 * qpg + qpg * d, nout = qpg * d;
-      const float *pb = P.part + ((size_t)in.b * P.nkv + in.g) * P.nchunk * PS;
-      for (int o0 = lane * 4; o0 < nout; o0 += 128) {
-        const int h = o0 / d;
-        float M = -INFINITY, den = 0.f;
-        float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (uint32_t c0 = 0; c0 < in.nchunk; c0 += 8) {
-          float mc[8], lc[8];
-          float4 oc[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            mc[u] = -INFINITY;
-            lc[u] = 0.f;
-            oc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c0 + u < in.nchunk) {
-              const float *pc = pb + (size_t)(c0 + u) * PS;
-              mc[u] = __ldcg(pc + h);
-              lc[u] = __ldcg(pc + qpg + h);
-              oc[u] = __ldcg(reinterpret_cast<const float4 *>(pc + 2 * qpg + o0));
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (mc[u] == -INFINITY) continue;
-            const float Mn = fmaxf(M, mc[u]);
-            const float a = __expf(M - Mn), w = __expf(mc[u] - Mn);
-            den = den * a + w * lc[u];
-            num.x = num.x * a + w * oc[u].x;
-            num.y = num.y * a + w * oc[u].y;
-            num.z = num.z * a + w * oc[u].z;
-            num.w = num.w * a + w * oc[u].w;
-            M = Mn;
-          }
-        }
-        const float inv = 1.f / den;
-        float *out = P.attn + (size_t)in.b * P.nq * d + (size_t)in.g * qpg * d + o0;
-        *reinterpret_cast<float4 *>(out) = make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-      }
-      __syncwarp();
-      if (lane == 0) red_release(ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
-    }
-  }
+  if (in.op != MK_OP_ATTN && lane == 0) red_release(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
   if (lane == 0) {
     red_add(P.exec + meta.idx, 1u);
     if (P.flags & MK_FLAG_TRACE) {

@@ -143,8 +143,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // ---- attention chunking ----------------------------------------------
   // A chunk holds at most one page of keys and one page of values, so its
   // instruction streams two pages and indexes rows without division.
+  // Automatic size: one page, halved (down to 64 positions) while the
+  // attention phase would occupy fewer than half of the SMs.
   const uint32_t rpp = page / (2 * (uint32_t)d);  // key (or value) rows per page
   uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : rpp;
+  if (c.attn_chunk <= 0)
+    while (ch > 64 && (uint64_t)B * nkv * cdiv(c.max_ctx, ch) < num_sms / 2) ch /= 2;
   if (ch % 16 || ch < 16 || ch > rpp)
     REJECT("attn_chunk must be a multiple of 16 and at most one page of keys");
   P.attn_chunk = ch;
