@@ -26,7 +26,11 @@
  *   activations h; ops 3, 5 -> residual rows; op 6 -> vocabulary rows.
  * An attention chunk adds 1 to its group's arrival counter; the chunk that
  *   brings that counter to sig2_after for the step (the last of the group)
- *   merges the group and adds 1 to sig2_ctr.
+ *   merges the group and adds 1 to sig2_ctr.  A projection may be split the
+ *   same way along its input dimension (batch > 1 plans): the slices of one
+ *   block of output rows (same op, layer and row0; chunk = slice index,
+ *   nchunk = slices) each add 1 to the block's arrival counter, and the last
+ *   one sums the slices, writes the rows and adds 1 to sig2_ctr.
  */
 #include <stdarg.h>
 #include <stdint.h>
@@ -176,7 +180,8 @@ int or_replay(const void *table, int N, int n_ctr, const or_shape *s, int S,
   ctx_t c;
   memset(&c, 0, sizeof c);
   c.N = N;
-  c.M = L * B * nkv;
+  const int M_att = L * B * nkv;  /* attention groups first, then split projections */
+  c.M = M_att + N;
   c.n_ctr = n_ctr;
   c.words = (N + c.M + 63) / 64;
   c.r = (rec_t *)calloc((size_t)N, sizeof(rec_t));
@@ -189,6 +194,11 @@ int or_replay(const void *table, int N, int n_ctr, const or_shape *s, int S,
   ilist *qkv_g = (ilist *)calloc((size_t)L * nkv, sizeof(ilist));
   unsigned char *cov_qkv = 0, *cov_h = 0, *cov_x3 = 0, *cov_x5 = 0, *cov_lm = 0, *cov_att = 0;
   uint32_t *nchunk_of = (uint32_t *)calloc((size_t)c.M, sizeof(uint32_t));
+  /* split projections: (op, layer, row0) -> group id, open addressing */
+  const size_t hcap = 2 * (size_t)N + 1;
+  uint64_t *hkey = (uint64_t *)calloc(hcap, sizeof(uint64_t));
+  int *hval = (int *)calloc(hcap, sizeof(int));
+  int n_split = 0;
 #define BYOP(op, l) byop[(op) * (L + 1) + (l)]
 
   /* 1. decode + field checks */
@@ -243,16 +253,44 @@ int or_replay(const void *table, int N, int n_ctr, const or_shape *s, int S,
       }
       push(&c.chunks[m], i);
     } else if (r->sig2_ctr != NONE) {
-      rc = fail(msg, msg_len, "instr %d: only attention chunks chain a second signal", i);
-      goto out;
+      if (r->nchunk == 0 || r->chunk >= r->nchunk || r->sig2_ctr >= (uint32_t)n_ctr ||
+          r->sig2_after != r->nchunk) {
+        rc = fail(msg, msg_len, "instr %d: bad split-projection fields", i);
+        goto out;
+      }
+      const uint64_t key = ((uint64_t)r->op << 56) | ((uint64_t)(uint32_t)r->layer << 32) | r->row0;
+      size_t h = (size_t)((key * 0x9E3779B97F4A7C15ULL) >> 20) % hcap;
+      while (hkey[h] && hkey[h] != key + 1) h = (h + 1) % hcap;
+      if (!hkey[h]) {
+        hkey[h] = key + 1;
+        hval[h] = n_split++;
+      }
+      int m = M_att + hval[h];
+      if (c.chunks[m].n == 0) nchunk_of[m] = r->nchunk;
+      if (nchunk_of[m] != r->nchunk || c.r[c.chunks[m].n ? c.chunks[m].v[0] : i].nrows != r->nrows) {
+        rc = fail(msg, msg_len, "instr %d: slices of one row block disagree", i);
+        goto out;
+      }
+      push(&c.chunks[m], i);
     }
   }
-  /* merge nodes: one per (layer, sequence, group); they signal sig2 */
-  for (int m = 0; m < c.M; ++m) {
+  /* merge nodes: one per (layer, sequence, group) of attention and one per
+     split row block; they signal sig2 */
+  for (int m = 0; m < M_att + n_split; ++m) {
     ilist *ch = &c.chunks[m];
     if ((uint32_t)ch->n != nchunk_of[m] || ch->n == 0) {
       rc = fail(msg, msg_len, "attention group %d has %d of %u chunks", m, ch->n, nchunk_of[m]);
       goto out;
+    }
+    if (m >= M_att) { /* slices must be 0..nchunk-1, each once */
+      unsigned char *seen = (unsigned char *)calloc(nchunk_of[m], 1);
+      int dup = 0;
+      for (int j = 0; j < ch->n; ++j) dup |= seen[c.r[ch->v[j]].chunk]++;
+      free(seen);
+      if (dup) {
+        rc = fail(msg, msg_len, "split row block %d: a slice appears twice", m - M_att);
+        goto out;
+      }
     }
     uint32_t sig2 = c.r[ch->v[0]].sig2_ctr, arr = c.r[ch->v[0]].sig_ctr;
     for (int j = 0; j < ch->n; ++j)
@@ -273,7 +311,7 @@ int or_replay(const void *table, int N, int n_ctr, const or_shape *s, int S,
   cov_x3 = (unsigned char *)calloc((size_t)L * s->H, 1);
   cov_x5 = (unsigned char *)calloc((size_t)L * s->H, 1);
   cov_lm = (unsigned char *)calloc((size_t)s->V, 1);
-  cov_att = (unsigned char *)calloc((size_t)c.M * 4096, 1);
+  cov_att = (unsigned char *)calloc((size_t)M_att * 4096, 1);
   for (int i = 0; i < N; ++i) {
     rec_t *r = &c.r[i];
     unsigned char *cov = 0;
@@ -297,6 +335,7 @@ int or_replay(const void *table, int N, int n_ctr, const or_shape *s, int S,
         continue;
       }
     }
+    if (r->sig2_ctr != NONE && r->chunk != 0) continue; /* a split block covers its rows once */
     if (r->nrows == 0 || r->row0 + r->nrows > lim) {
       rc = fail(msg, msg_len, "instr %d: rows [%u,%u) outside [0,%u)", i, r->row0,
                 r->row0 + r->nrows, lim);
@@ -432,6 +471,8 @@ out:
   free_lists(byop, 7 * (L + 1));
   free_lists(qkv_g, L * nkv);
   free(nchunk_of);
+  free(hkey);
+  free(hval);
   free(cov_qkv);
   free(cov_h);
   free(cov_x3);
@@ -457,7 +498,7 @@ static uint64_t rng_next(uint64_t *s) {
 
 static void apply_done(const rec_t *r, uint32_t *cnt) {
   cnt[r->sig_ctr] += 1;
-  if (r->op == OATTN && cnt[r->sig_ctr] == r->sig2_after) cnt[r->sig2_ctr] += 1;
+  if (r->sig2_ctr != NONE && cnt[r->sig_ctr] == r->sig2_after) cnt[r->sig2_ctr] += 1;
 }
 
 static int ready(const rec_t *r, const uint32_t *cnt) {

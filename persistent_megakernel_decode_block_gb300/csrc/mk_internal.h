@@ -38,6 +38,10 @@ constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2;
 // per lane.
 struct OpGeom {
   uint32_t K, NS, SW, item_bytes, ipp, nch;
+  // batch > 1 (tensor-core) plans: tiles of MR weight rows x KS input
+  // columns (S = K / KS slices per block of rows), pages of MR rows x kc
+  // columns in the MMA's core-matrix order, ppt pages per tile
+  uint32_t MR, KS, S, kc, ppt;
 };
 
 struct KParams {
@@ -58,6 +62,8 @@ struct KParams {
   OpGeom geom[8];
   int32_t L, H, nq, nkv, d, F, V, B, max_ctx, qpg;
   int32_t nchunk, attn_chunk, att_lmax;
+  int32_t tc, tc_nb;  // tensor-core projections (batch > 1); MMA N = 2 x batch rounded up to 16
+  float *gpart;       // partial sums of split projections [block][slice][MR][B]
   float eps, attn_scale;
   int32_t n_wait, mode;
   uint32_t range_first, range_count, n_blocks, flags;
@@ -85,6 +91,8 @@ cudaError_t set_megakernel_smem(uint32_t bytes);
 cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
                               cudaStream_t stream);
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream);
+cudaError_t launch_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             uint32_t nrows, const OpGeom &g, uint32_t page, cudaStream_t stream);
 cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
                           const uint64_t *rowtab, uint32_t nrows, const OpGeom &g, uint32_t page,
                           cudaStream_t stream);

@@ -73,6 +73,49 @@ DEVI bool mbar_test(uint64_t *b, uint32_t parity) {
 DEVI void bulk_prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// ---- tcgen05 (5th-generation tensor cores, accumulator in tensor memory) ----
+// Shared-memory matrix descriptor: start address, byte strides between 8-row
+// x 16-byte core matrices along K (lbo) and along M/N (sbo), no swizzle.
+DEVI uint64_t tc_desc(uint32_t saddr_bytes, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr_bytes >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 and M >> 4.
+DEVI uint32_t tc_idesc(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+DEVI void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// arrives once on `bar` when every tensor-core operation this thread issued
+// before it has completed
+DEVI void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   saddr(bar))
+               : "memory");
+}
+DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+DEVI void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// 32 lanes x 16 columns of 32-bit words (this warp's lane quarter)
+DEVI void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 DEVI uint64_t policy_evict_first() {
   uint64_t p;
@@ -143,7 +186,7 @@ DEVI float warp_max(float v) {
 // ------------------------------------------------------- shared state ----
 struct Smem {
   uint8_t *ring;
-  uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar;
+  uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar, *tbar, *dbar;
   mk_instr *fifo;
   SlotMeta *meta;
   float *res, *opart, *ml, *sc, *rope, *normr, *rbuf, *xs;
@@ -167,6 +210,8 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.done = S.rdy + kFifo;
   S.attbar = S.done + kFifo;
   S.xbar = S.attbar + 1;
+  S.tbar = S.xbar + 1;  // tensor-core results of a tile ready
+  S.dbar = S.tbar + 1;  // every tensor-core operation drained (kernel end)
   S.fifo = reinterpret_cast<mk_instr *>(base + P.off_fifo);
   S.meta = reinterpret_cast<SlotMeta *>(base + P.off_meta);
   S.res = reinterpret_cast<float *>(base + P.off_res);
@@ -264,6 +309,11 @@ DEVI uint32_t n_pages(const KParams &P, const Smem &S, const mk_instr &in) {
 
 DEVI void page_src(const KParams &P, const Smem &S, const mk_instr &in, uint32_t p,
                    uint32_t np, const void *&src, uint32_t &bytes) {
+  if (in.op != MK_OP_ATTN && P.tc) {  // tensor-core tiles are whole pages
+    src = P.arena + in.wofs + (uint64_t)p * P.page_bytes;
+    bytes = P.page_bytes;
+    return;
+  }
   if (in.op != MK_OP_ATTN) {
     const OpGeom &G = P.geom[in.op];
     const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
@@ -643,20 +693,20 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
   const OpGeom &G = P.geom[in.op];
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const bool norm = gain_of(P, in.op, in.layer) != nullptr;
-  if (cw < P.B) {
+  for (int b = cw; b < P.B; b += kComputeWarps) {  // a warp per sequence
     float r = 1.f;
     if (norm) {
       float ss = 0.f;
       for (uint32_t c = lane * 8; c < G.K; c += 256) {
         float v[8];
-        load8(P, S, in.op, emb, cw, c, v);
+        load8(P, S, in.op, emb, b, c, v);
 #pragma unroll
         for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
       }
       ss = warp_sum(ss);
       r = rsqrtf(ss / (float)G.K + P.eps);
     }
-    if (lane == 0) normr[cw] = r;
+    if (lane == 0) normr[b] = r;
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(S.xbar);
@@ -716,20 +766,102 @@ DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const Slo
   return true;
 }
 
-// Batch > 1 GEMV of one instruction: every item is dotted with the B input
-// rows (read through L2), the gains folded into the weights and 1/rms
-// applied at the end.
-__device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
-                  float *res, int cw, int lane, uint32_t &xkey, uint32_t &xbar_uses,
-                  uint32_t &key_changes) {
+
+// ---------------------------------------------- batch > 1: tensor cores ----
+// The epilogue of a split projection block, run by the compute threads of the
+// block's last slice: out(r, b) = the sum over slices, in slice order, of the
+// slices' partial sums; then RoPE and the KV append (q/k/v rows), the
+// residual (O, down), SiLU(gate) * up, or the logits.
+__device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
+                                         int tid) {
   const OpGeom &G = P.geom[in.op];
-  const uint32_t wrows = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
-  const uint32_t items = wrows * G.NS;
-  const uint32_t A = G.NS * (kComputeWarps / G.NS);
-  const bool active = (uint32_t)cw < A;
-  const uint32_t s = cw % G.NS;
+  const int B = P.B, MR = (int)G.MR, NSL = (int)in.nchunk, d = P.d;
+  const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
+  const float *gp = P.gpart + (size_t)rb * NSL * MR * B;
+  auto val = [&](int r, int b) {
+    float v = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < NSL; ++s) v += __ldcg(gp + ((size_t)s * MR + r) * B + b);
+    return v;
+  };
+  constexpr int T = kComputeWarps * 32;
+  switch (in.op) {
+    case MK_OP_QKV: {
+      const int GR = (P.qpg + 2) * d, half = d / 2, npairs = (int)in.nrows / 2;
+      for (int u = tid; u < npairs * B; u += T) {
+        const int pr = u % npairs, b = u / npairs;
+        const int R = (int)in.row0 + 2 * pr, grp = R / GR, q = R % GR;
+        const float x0 = val(2 * pr, b), x1 = val(2 * pr + 1, b);
+        if (q < (P.qpg + 1) * d) {
+          const int i = (q % d) / 2;
+          const float cs = S.rope[b * d + i], sn = S.rope[b * d + half + i];
+          const float o0 = x0 * cs - x1 * sn, o1 = x0 * sn + x1 * cs;
+          if (q < P.qpg * d) {
+            float *qd = P.q + ((size_t)b * P.nq + grp * P.qpg + q / d) * d;
+            qd[i] = o0;
+            qd[i + half] = o1;
+          } else {
+            uint16_t *kd = P.kc + kv_row(P, in.layer, b, grp, S.pos[b]);
+            kd[i] = to_bf(o0);
+            kd[i + half] = to_bf(o1);
+          }
+        } else {
+          uint16_t *vd = P.vc + kv_row(P, in.layer, b, grp, S.pos[b]) + (q - (P.qpg + 1) * d);
+          vd[0] = to_bf(x0);
+          vd[1] = to_bf(x1);
+        }
+      }
+      break;
+    }
+    case MK_OP_OPROJ:
+    case MK_OP_DOWN:
+      for (int u = tid; u < (int)in.nrows * B; u += T) {
+        const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
+        const float resid = (in.op == MK_OP_OPROJ && (in.flags & 1))
+                                ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
+                                : __ldcg(P.x + (size_t)b * P.H + row);
+        P.x[(size_t)b * P.H + row] = resid + val(r, b);
+      }
+      break;
+    case MK_OP_GATEUP:
+      for (int u = tid; u < (int)in.nrows * B; u += T) {
+        const int j = u % in.nrows, b = u / in.nrows;
+        const float gt = val(j, b), up = val(MR / 2 + j, b);
+        P.h[(size_t)b * P.F + in.row0 + j] = gt / (1.f + __expf(-gt)) * up;
+      }
+      break;
+    default:  // LM head
+      for (int u = tid; u < (int)in.nrows * B; u += T) {
+        const int r = u % in.nrows, b = u / in.nrows;
+        P.logits[(size_t)b * P.V + in.row0 + r] = val(r, b);
+      }
+      break;
+  }
+}
+
+// One batch > 1 projection tile: MR weight rows x KS input columns (slice
+// `chunk` of `nchunk`), on the tensor cores.
+//  1. The compute warps stage the MMA's B operand: the slice of the B
+//     (normalised) input rows as bf16 values in rows 0..B-1 and as bf16
+//     remainders x - bf16(x) in rows B..2B-1, so value plus remainder keep
+//     about 16 significant bits of the fp32 input.
+//  2. Compute warp 0 lane 0 issues the MMAs (A = the ring page, K-major,
+//     fp32 accumulator in tensor memory) page by page as pages land; a commit
+//     releases each page once its MMAs are done (the other warps' arrivals
+//     make up the rest of the page's release count).
+//  3. The four warps whose ids cover the four lane quarters of tensor memory
+//     read the MR x N accumulator and write value + remainder column, the
+//     tile's partial sums, to global memory.
+//  4. The slice that completes its block (acq_rel arrival) runs tc_epilogue
+//     with every compute thread and releases the phase counter.
+__device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_instr &in,
+                                     const SlotMeta &meta, int cw, int lane, uint32_t epoch,
+                                     uint32_t &xkey, uint32_t &xbar_uses, uint32_t &key_changes,
+                                     uint32_t &tc_uses) {
+  const OpGeom &G = P.geom[in.op];
+  const int B = P.B, NB = P.tc_nb, MR = (int)G.MR, KS = (int)G.KS;
+  const int tid = cw * 32 + lane;
   const uint32_t key = input_key(in);
-  const int B = P.B;
   if (key != xkey) {
     ++key_changes;
     if (!norm_factors(P, S, in, cw, lane, xbar_uses, S.normr + (key_changes & 1u) * kMaxBatch))
@@ -739,47 +871,88 @@ __device__ __noinline__ bool gemv_bn(const KParams &P, const Smem &S, const mk_i
   const float *normr = S.normr + (key_changes & 1u) * kMaxBatch;
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const uint16_t *gain = gain_of(P, in.op, in.layer);
-  const uint32_t E = P.ring_pages;
-  uint32_t item = cw;
+  uint8_t *bop = reinterpret_cast<uint8_t *>(S.xs);
+  const int c0 = (int)in.chunk * KS;
+  // 1. B operand (rows >= 2B stay zero from the kernel's start)
+  for (int t = tid; t < B * (KS / 8); t += kComputeWarps * 32) {
+    const int b = t / (KS / 8), k = (t % (KS / 8)) * 8;
+    float v[8], g8[8];
+    load8(P, S, in.op, emb, b, c0 + k, v);
+    if (gain) load_gain8(gain, c0 + k, g8);
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 8; u += 2) {
+      const float x0 = v[u] * normr[b] * (gain ? g8[u] : 1.f);
+      const float x1 = v[u + 1] * normr[b] * (gain ? g8[u + 1] : 1.f);
+      const uint16_t h0 = to_bf(x0), h1 = to_bf(x1);
+      const uint16_t l0 = to_bf(x0 - bf1(h0)), l1 = to_bf(x1 - bf1(h1));
+      hi[u / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      lo[u / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    const int kb = (k / 16) * (NB * 32) + ((k / 8) % 2) * 128;
+    *reinterpret_cast<uint4 *>(bop + kb + (b / 8) * 256 + (b % 8) * 16) =
+        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4 *>(bop + kb + ((B + b) / 8) * 256 + ((B + b) % 8) * 16) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+  fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
+  if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+  // 2. MMAs
+  const uint32_t E = P.ring_pages, taddr = (uint32_t)S.misc[3];
+  const uint32_t idesc = tc_idesc((uint32_t)MR, (uint32_t)NB), bbase = saddr(bop);
+  if (cw == 0 && lane == 0) tc_fence_after();
   for (uint32_t p = 0; p < meta.npages; ++p) {
     const uint32_t seq = meta.seq0 + p, slot = seq % E;
     if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
-    const uint8_t *page = S.ring + (size_t)slot * P.page_bytes;
-    const uint32_t it_end = min(items, (p + 1) * G.ipp);
-    for (; active && item < it_end; item += A) {
-      const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
-      float acc[kMaxBatch];
-#pragma unroll
-      for (int b = 0; b < kMaxBatch; ++b) acc[b] = 0.f;
-      for (uint32_t j = 0; j < G.nch; ++j) {
-        const int col = s * G.SW + j * 256 + lane * 8;
-        const uint4 w = *reinterpret_cast<const uint4 *>(ip + j * 512 + lane * 16);
-        float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                       bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-        if (gain) {
-          float g8[8];
-          load_gain8(gain, col, g8);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) wf[t] *= g8[t];
-        }
-#pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b)
-          if (b < B) {
-            float v[8];
-            load8(P, S, in.op, emb, b, col, v);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) acc[b] = fmaf(wf[t], v[t], acc[b]);
-          }
+    if (cw == 0) {
+      if (lane == 0) {
+        const uint32_t abase = saddr(S.ring + (size_t)slot * P.page_bytes);
+        for (uint32_t t = 0; t < G.kc / 16; ++t)
+          tc_mma(taddr, tc_desc(abase + t * (uint32_t)MR * 32, 128, 256),
+                 tc_desc(bbase + (p * (G.kc / 16) + t) * (uint32_t)NB * 32, 128, 256), idesc,
+                 (p | t) != 0);
+        tc_commit(&S.empty[slot]);
       }
+      __syncwarp();
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+    }
+  }
+  if (cw == 0 && lane == 0) tc_commit(S.tbar);
+  // 3. accumulator -> partial sums (warp w of the block reads lanes 32 (w % 4) ..)
+  if (cw >= 2 && cw < 6) {
+    const int qd = (cw + 2) % 4;
+    if (!warp_wait(P, S, S.tbar, tc_uses & 1u, kWhereCompute | meta.idx)) return false;
+    if (32 * qd < MR) {
+      tc_fence_after();
+      float v[32];
+      float(&v0)[16] = *reinterpret_cast<float(*)[16]>(v);
+      float(&v1)[16] = *reinterpret_cast<float(*)[16]>(v + 16);
+      const uint32_t ta = taddr + ((uint32_t)(32 * qd) << 16);
+      tc_ld16(ta, v0);
+      if (NB > 16) tc_ld16(ta + 16, v1);
+      const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
+      const int r = 32 * qd + lane;
+      float *dst = P.gpart + (((size_t)rb * in.nchunk + in.chunk) * MR + r) * B;
 #pragma unroll
       for (int b = 0; b < kMaxBatch; ++b)
-        if (b < B) {
-          const float a = warp_sum(acc[b]) * normr[b];
-          if (lane == 0) res[item * B + b] = a;
-        }
+        if (b < B) dst[b] = v[b] + v[B + b];
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
+  }
+  ++tc_uses;
+  tc_fence_before();
+  if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+  // 4. arrival; the block's last slice sums the slices and finishes the rows
+  if (cw == 0 && lane == 0) {
+    const uint32_t old = atom_add_acq_rel(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+    S.misc[2] = old == epoch * in.nchunk + in.nchunk - 1u ? 1 : 0;
+  }
+  if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+  if (S.misc[2]) {
+    tc_epilogue(P, S, in, tid);
+    if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+    if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
   }
   return true;
 }
@@ -1139,7 +1312,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
 }
 
 DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int lane) {
-  uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu;
+  uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu, tc_uses = 0;
   uint32_t fs = 0;
   if (!next_entry(P, S, fs)) return;
   while (true) {
@@ -1155,13 +1328,12 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       continue;
     }
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return;
-    float *res = S.res + (size_t)f * P.res_floats;
     bool ok;
     if (in.op == MK_OP_ATTN) {
       ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses, epoch);
       xkey = 0xFFFFFFFFu;
     } else {
-      ok = gemv_bn(P, S, in, meta, res, cw, lane, xkey, xbar_uses, key_changes);
+      ok = gemv_tc(P, S, in, meta, cw, lane, epoch, xkey, xbar_uses, key_changes, tc_uses);
     }
     if (!ok) return;
     finish_entry(P, S, fs, cw, lane);
@@ -1181,7 +1353,9 @@ DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
     return v;
   };
   uint32_t *ctr = P.ctr;
-  switch (in.op) {
+  // batch > 1 projections finish (and signal) on the compute warps
+  const bool compute_owned = in.op == MK_OP_ATTN || P.tc;
+  if (!compute_owned) switch (in.op) {
     case MK_OP_QKV: {
       // rows come in pairs: one RoPE rotation pair (natural dims i and
       // i + d/2) of a q head or of k, or two consecutive v dims
@@ -1244,7 +1418,7 @@ DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
   // warp by the slot's done barrier)
   // (attention chunks signal and merge from the compute warps)
   __syncwarp();
-  if (in.op != MK_OP_ATTN && lane == 0) red_release(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+  if (!compute_owned && lane == 0) red_release(ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
   if (lane == 0) {
     red_add(P.exec + meta.idx, 1u);
     if (P.flags & MK_FLAG_TRACE) {
@@ -1285,7 +1459,7 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
     const SlotMeta &meta = S.meta[f];
     if (in.op == MK_OP_END) break;
     if (!warp_wait(P, S, &S.rdy[f], k & 1u, kWhereStorer)) break;
-    prefetch_residual(P, S, in, lane);
+    if (!P.tc) prefetch_residual(P, S, in, lane);
     if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
     if (lane == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[f].t_sstart = gtimer();
     __syncwarp();
@@ -1320,6 +1494,8 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(S.attbar, kComputeWarps);
     mbar_init(S.xbar, kComputeWarps);
+    mbar_init(S.tbar, 1);
+    mbar_init(S.dbar, 1);
     fence_mbar_init();
     S.misc[0] = 0;
     S.misc[1] = 0;
@@ -1349,6 +1525,24 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && blockIdx.x == 0) raise_error(P, MK_ERR_BOUNDS, 0, false);
     return;
   }
+  if (P.tc) {
+    // tensor memory for the projections' accumulator (at most 32 fp32
+    // columns), and a zeroed B-operand buffer (rows past 2B stay zero)
+    if (warp == 2) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(
+                       saddr((const void *)(S.misc + 3)))
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    uint32_t bop_bytes = 0;
+    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
+      if (op != MK_OP_ATTN) bop_bytes = max(bop_bytes, P.geom[op].KS * (uint32_t)P.tc_nb * 2u);
+    for (uint32_t i = tid; i < bop_bytes / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(S.xs)[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (warp == 0) {
     if (lane == 0) loader(P, S, epoch);
     __syncwarp();
@@ -1358,6 +1552,25 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     compute(P, S, epoch, warp - 2, lane);
   }
   __syncthreads();
+  if (P.tc) {
+    // every tensor-core operation (issued by compute warp 0 lane 0) is done
+    // before the accumulator's tensor memory is freed
+    if (warp == 2 && lane == 0) {
+      tc_commit(S.dbar);
+      const uint64_t t0 = cycles();
+      while (!mbar_try_wait(S.dbar, 0u))
+        if (cycles() - t0 > P.timeout_cycles) {
+          raise_error(P, MK_ERR_TIMEOUT, kWhereDrain | 0xFFFFFFu, true);
+          break;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"((uint32_t)S.misc[3])
+                   : "memory");
+  }
   // a block only bails after a latched error; never let it end silently
   if (tid == 0 && S.misc[0] != 0) raise_error(P, MK_ERR_TIMEOUT, 0x0FFFFFFFu, true);
   if (tid == 0 && P.mode != kModeRange && S.misc[0] == 0) {
@@ -1396,6 +1609,30 @@ extern "C" __global__ void mk_retile(uint8_t *dst, const uint8_t *src, const int
   }
 }
 
+// Tensor-core tiles (batch > 1 plans): weight row k (source row map[k]) and
+// 8 columns from c go to block rb = k / MR (row rr = k % MR), slice c / KS,
+// page (c % KS) / kc of the slice, and inside the page to the core matrix
+// (rr / 8, (cc / 8) % 2) of k-step cc / 16, cc = c % kc: the MMA reads a
+// k-step as MR x 16 bf16 in 8-row x 16-byte core matrices, 128 bytes apart
+// along K and 256 bytes apart along M.
+extern "C" __global__ void mk_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                                        uint32_t nrows, uint32_t K, uint32_t MR, uint32_t KS,
+                                        uint32_t S, uint32_t kc, uint32_t ppt, uint32_t page) {
+  const uint64_t per_row = K / 8;
+  const uint64_t total = (uint64_t)nrows * per_row;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = (uint32_t)(i / per_row);
+    const uint32_t c = (uint32_t)(i % per_row) * 8;
+    const uint32_t rb = k / MR, rr = k % MR, sl = c / KS, j = (c % KS) / kc, cc = c % kc;
+    uint8_t *d = dst + (((uint64_t)rb * S + sl) * ppt + j) * page + (cc / 16) * (MR * 32) +
+                 (rr / 8) * 256 + ((cc / 8) % 2) * 128 + (rr % 8) * 16;
+    const uint32_t srow = map ? (uint32_t)map[k] : k;
+    *reinterpret_cast<uint4 *>(d) =
+        *reinterpret_cast<const uint4 *>(src + (uint64_t)srow * K * 2 + (uint64_t)c * 2);
+  }
+}
+
 // ---- host-side launch helpers (the kernels' host stubs live in this unit) ----
 cudaError_t set_megakernel_smem(uint32_t bytes) {
   return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1419,6 +1656,15 @@ cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
 
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream) {
   mk_epoch_advance<<<1, 1, 0, stream>>>(ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             uint32_t nrows, const OpGeom &g, uint32_t page, cudaStream_t stream) {
+  const uint64_t total = (uint64_t)nrows * g.K / 8;
+  const uint32_t blocks = (uint32_t)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
+  mk_retile_tc<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, nrows, g.K, g.MR, g.KS, g.S,
+                                                         g.kc, g.ppt, page);
   return cudaGetLastError();
 }
 

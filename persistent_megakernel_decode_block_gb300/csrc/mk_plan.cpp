@@ -116,9 +116,46 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.tiles[MK_OP_GATEUP] = split(F, 1, S_, 2 * P.geom[MK_OP_GATEUP].NS);
   P.tiles[MK_OP_DOWN] = split(H, 1, S_, P.geom[MK_OP_DOWN].NS);
   P.tiles[MK_OP_LMHEAD] = split(V, lm_unit, S_, P.geom[MK_OP_LMHEAD].NS);
-  if (too_big) REJECT("a GEMV tile has too many items");
+  if (too_big && B == 1) REJECT("a GEMV tile has too many items");
+  // Batch > 1: every projection runs on the tensor cores (tcgen05, M = MR
+  // weight rows, N = the batch's values and bf16 remainders).  A block of MR
+  // rows is split along K into S slices of KS columns so that a phase has at
+  // least as many tiles as SMs; the last slice of a block to finish sums the
+  // slices (in slice order) and applies the epilogue.
+  P.tc = B > 1;
+  if (P.tc) {
+    P.tc_nb = 16 * cdiv(2 * (uint32_t)B, 16);
+    const uint32_t rows_of[8] = {0, (uint32_t)(nkv * GR), 0, (uint32_t)H, (uint32_t)(2 * F),
+                                 (uint32_t)H, (uint32_t)V, 0};
+    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
+      if (op == MK_OP_ATTN) continue;
+      OpGeom &g = P.geom[op];
+      g.MR = (op == MK_OP_QKV && GR % 128) ? 64 : 128;
+      g.kc = page / (g.MR * 2);
+      if (g.kc < 16 || g.kc % 16) REJECT("page too small for a tensor-core tile");
+      const uint32_t blocks = cdiv(rows_of[op], g.MR);
+      uint32_t ks = 512;
+      while (ks > g.kc && (g.K % ks || ks > g.K)) ks /= 2;
+      while (ks > g.kc && (uint64_t)blocks * (g.K / ks) < num_sms) ks /= 2;
+      if (ks % g.kc || g.K % ks) REJECT("input width does not split into tensor-core pages");
+      g.KS = ks;
+      g.S = g.K / ks;
+      g.ppt = ks / g.kc;
+      // outputs of each block (gate/up: MR/2 outputs = MR weight rows)
+      const uint32_t per = op == MK_OP_GATEUP ? g.MR / 2 : g.MR;
+      const uint32_t nout = op == MK_OP_QKV ? (uint32_t)GR : op == MK_OP_GATEUP ? (uint32_t)F
+                            : op == MK_OP_LMHEAD ? (uint32_t)V : (uint32_t)H;
+      P.tiles[op].clear();
+      for (uint32_t r0 = 0; r0 < nout; r0 += per) P.tiles[op].push_back(std::min(per, nout - r0));
+      P.gpart_floats = std::max<uint64_t>(P.gpart_floats,
+                                          (uint64_t)blocks * g.S * g.MR * (uint32_t)B);
+    }
+  }
   auto wrows_of = [](int op, uint32_t n) { return op == MK_OP_GATEUP ? 2 * n : n; };
-  auto tile_pages = [&](int op, uint32_t wrows) { return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp); };
+  auto tile_pages = [&](int op, uint32_t wrows) {
+    if (P.tc) return P.geom[op].ppt;
+    return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp);
+  };
   uint32_t tile_items_max = 0;
   for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
     for (uint32_t n : P.tiles[op])
@@ -134,6 +171,10 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     for (int g = 0; g < reps; ++g)
       for (uint32_t n : P.tiles[op]) {
         const uint32_t w = wrows_of(op, n);
+        if (P.tc) {  // tensor-core tiles: S slices of ppt pages; retiled by formula
+          toff += (uint64_t)P.geom[op].S * P.geom[op].ppt * page;
+          continue;
+        }
         for (uint32_t r = 0; r < w; ++r) rt.push_back(toff | r);
         toff += (uint64_t)tile_pages(op, w) * page;
       }
@@ -162,6 +203,13 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   const uint32_t arr_base = P.n_wait;
   P.lm_ctr = arr_base + (uint32_t)L * B * nkv;
   P.n_ctr = P.lm_ctr + 1;
+  // split row blocks of tensor-core plans: one arrival counter each
+  P.gemv_arr_base = P.n_ctr;
+  if (P.tc)
+    P.n_ctr += (uint32_t)L * (uint32_t)(nkv * P.tiles[MK_OP_QKV].size() + P.tiles[MK_OP_OPROJ].size() +
+                                        P.tiles[MK_OP_GATEUP].size() + P.tiles[MK_OP_DOWN].size()) +
+               (uint32_t)P.tiles[MK_OP_LMHEAD].size();
+  uint32_t next_arr = P.gemv_arr_base;
   P.ctr_inc.assign(P.n_ctr, 0);
 
   // ---- weight arena: norms, embedding, then tiles in queue order ---------
@@ -175,7 +223,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     bool plain = page % g.item_bytes == 0;
     const std::vector<uint32_t> &t = P.tiles[MK_OP_LMHEAD];
     for (size_t i = 0; i + 1 < t.size(); ++i) plain = plain && (t[i] * g.NS) % g.ipp == 0;
-    P.embed_alias = c.tie_embeddings && plain;
+    P.embed_alias = c.tie_embeddings && plain && !P.tc;
   }
   if (!P.embed_alias) {
     P.off_embed = off;
@@ -211,21 +259,44 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.off_gu.resize(L);
   P.off_d.resize(L);
 
-  auto gemv_tiles = [&](uint8_t op, mk_instr proto) {
+  // one tile per entry of P.tiles[op], or, in tensor-core plans, S slices of
+  // it chained through the block's arrival counter to the phase counter
+  auto emit_tile = [&](uint8_t op, mk_instr in) {
     const OpGeom &g = P.geom[op];
+    const uint32_t wrows = wrows_of(op, in.nrows);
+    P.weight_bytes += (uint64_t)wrows * g.K * 2;
+    if (!P.tc) {
+      in.npages = tile_pages(op, wrows);
+      in.wofs = off;
+      off += (uint64_t)in.npages * page;
+      push(in);
+      P.ctr_inc[in.sig_ctr]++;
+      return;
+    }
+    const uint32_t phase_ctr = in.sig_ctr, arr = next_arr++;
+    for (uint32_t sl = 0; sl < g.S; ++sl) {
+      mk_instr t = in;
+      t.sig_ctr = arr;
+      t.sig2_ctr = phase_ctr;
+      t.sig2_after = g.S;
+      t.chunk = sl;
+      t.nchunk = g.S;
+      t.npages = g.ppt;
+      t.wofs = off;
+      off += (uint64_t)g.ppt * page;
+      push(t);
+      P.ctr_inc[arr]++;
+    }
+    P.ctr_inc[phase_ctr]++;
+  };
+  auto gemv_tiles = [&](uint8_t op, mk_instr proto) {
     uint32_t row0 = 0;
     for (uint32_t n : P.tiles[op]) {
       mk_instr in = proto;
       in.row0 = row0;
       in.nrows = n;
-      const uint32_t wrows = wrows_of(op, n);
-      in.npages = tile_pages(op, wrows);
-      in.wofs = off;
-      off += (uint64_t)in.npages * page;
       row0 += n;
-      P.weight_bytes += (uint64_t)wrows * g.K * 2;
-      push(in);
-      P.ctr_inc[in.sig_ctr]++;
+      emit_tile(op, in);
     }
   };
 
@@ -233,29 +304,21 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     // RMSNorm + QKV + RoPE, group-major so a group's attention can start early
     new_phase(MK_OP_QKV, l);
     P.off_qkv[l] = off;
-    {
-      const OpGeom &g = P.geom[MK_OP_QKV];
-      for (int grp = 0; grp < nkv; ++grp) {
-        uint32_t r0 = 0;
-        for (uint32_t n : P.tiles[MK_OP_QKV]) {
-          mk_instr in = base(MK_OP_QKV, l);
-          in.flags = l == 0 ? 1 : 0;
-          in.g = (uint16_t)grp;
-          if (l > 0) {
-            in.wait_ctr = ctr_d(c, l - 1);
-            in.wait_tgt = nD;
-          }
-          in.sig_ctr = ctr_qkv(c, l, grp);
-          in.row0 = grp * GR + r0;
-          in.nrows = n;
-          in.npages = tile_pages(MK_OP_QKV, n);
-          in.wofs = off;
-          off += (uint64_t)in.npages * page;
-          r0 += n;
-          P.weight_bytes += (uint64_t)n * g.K * 2;
-          push(in);
-          P.ctr_inc[in.sig_ctr]++;
+    for (int grp = 0; grp < nkv; ++grp) {
+      uint32_t r0 = 0;
+      for (uint32_t n : P.tiles[MK_OP_QKV]) {
+        mk_instr in = base(MK_OP_QKV, l);
+        in.flags = l == 0 ? 1 : 0;
+        in.g = (uint16_t)grp;
+        if (l > 0) {
+          in.wait_ctr = ctr_d(c, l - 1);
+          in.wait_tgt = nD;
         }
+        in.sig_ctr = ctr_qkv(c, l, grp);
+        in.row0 = grp * GR + r0;
+        in.nrows = n;
+        r0 += n;
+        emit_tile(MK_OP_QKV, in);
       }
     }
     // attention chunks, group-major
@@ -362,7 +425,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
 
   // ---- shared-memory layout -------------------------------------------------
   // per-slot dot products (items x batch); also the size of the storer's residual buffer
-  P.res_floats = (uint32_t)align_up((uint64_t)tile_items_max * B, 4);
+  P.res_floats = P.tc ? 4u : (uint32_t)align_up((uint64_t)tile_items_max * B, 4);
   uint32_t fixed = 0;
   auto take = [&](uint32_t bytes, uint32_t align) {
     fixed = (uint32_t)align_up(fixed, align);
@@ -385,9 +448,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
   uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
   // staged GEMV input (normalised x, or the attention output) and attention scores
-  const uint32_t xs_floats = std::max<uint32_t>(H, QD);
+  uint32_t xs_floats = std::max<uint32_t>(H, QD);
+  if (P.tc)  // the MMA's B operand of one tile: KS x N bf16
+    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
+      if (op != MK_OP_ATTN) xs_floats = std::max<uint32_t>(xs_floats, P.geom[op].KS * P.tc_nb / 2);
   uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
-  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 2) * 8;
+  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4) * 8;
   uint32_t rel_bars = take(bars_max, 8);
   uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
   uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);

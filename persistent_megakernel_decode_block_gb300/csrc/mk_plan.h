@@ -28,6 +28,10 @@ struct HostPlan {
   bool embed_alias = false;  // embedding rows read from the LM-head block
   uint32_t n_wait = 0, n_ctr = 0, lm_ctr = 0;
   uint32_t attn_chunk = 0, nchunk = 0, att_lmax = 0;
+  bool tc = false;              // batch > 1: projections on tcgen05, split along K
+  uint32_t tc_nb = 0;           // MMA N: 2 x batch (value and remainder) rounded up to 16
+  uint64_t gpart_floats = 0;    // partial-sum buffer of split projections
+  uint32_t gemv_arr_base = 0;   // arrival counters of split row blocks
   // shared-memory layout
   uint32_t ring_pages = 0, page_bytes = 0, res_floats = 0;
   uint32_t off_bars = 0, off_fifo = 0, off_meta = 0, off_res = 0, off_att = 0, off_sat = 0,

@@ -24,7 +24,7 @@ struct mk_plan_s {
            *d_exec = nullptr, *d_ctr_inc = nullptr;
   unsigned long long *d_trace = nullptr;
   float *d_x = nullptr, *d_q = nullptr, *d_attn = nullptr, *d_h = nullptr, *d_part = nullptr,
-        *d_cos = nullptr, *d_sin = nullptr, *d_logits_stage = nullptr;
+        *d_cos = nullptr, *d_sin = nullptr, *d_logits_stage = nullptr, *d_gpart = nullptr;
   int32_t *d_tok_stage = nullptr, *d_pos_stage = nullptr, *d_qkv_map = nullptr,
           *d_gu_map = nullptr;
   bool weights_loaded = false;
@@ -83,7 +83,7 @@ static void free_device(mk_plan_s *p) {
                   p->d_ctrl, p->d_exec, p->d_ctr_inc, p->d_trace, p->d_x,
                   p->d_q, p->d_attn, p->d_h, p->d_part, p->d_cos,
                   p->d_sin, p->d_logits_stage, p->d_tok_stage, p->d_pos_stage, p->d_qkv_map,
-                  p->d_gu_map};
+                  p->d_gu_map, p->d_gpart};
   for (void *q : ptrs)
     if (q) cudaFree(q);
 }
@@ -129,6 +129,7 @@ static int setup_device(mk_plan_s *p) {
   AL(p->d_pos_stage, (size_t)B);
   AL(p->d_qkv_map, H.qkv_map.size());
   AL(p->d_gu_map, H.gu_map.size());
+  if (H.tc) AL(p->d_gpart, H.gpart_floats);
 #undef AL
   CK(cudaMemcpy(p->d_instr, H.instr.data(), N * sizeof(mk_instr), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(p->d_list_off, H.list_off.data(), H.list_off.size() * 4, cudaMemcpyHostToDevice));
@@ -191,6 +192,9 @@ static int setup_device(mk_plan_s *p) {
   P.nchunk = (int32_t)H.nchunk;
   P.attn_chunk = (int32_t)H.attn_chunk;
   P.att_lmax = (int32_t)H.att_lmax;
+  P.tc = H.tc ? 1 : 0;
+  P.tc_nb = (int32_t)H.tc_nb;
+  P.gpart = p->d_gpart;
   P.eps = c.rms_eps;
   P.attn_scale = (float)(1.0 / sqrt((double)d));
   P.n_wait = (int32_t)H.n_wait;
@@ -380,8 +384,13 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
   uint8_t *A = p->d_arena;
   auto norm_dst = [&](int idx) { return A + H.off_norms + (size_t)idx * H_ * 2; };
   auto retile = [&](uint8_t *dst, const int32_t *map, uint32_t rows, int op) {
-    if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
-    cudaError_t e = launch_retile(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], pg, s);
+    cudaError_t e;
+    if (H.tc) {
+      e = launch_retile_tc(dst, stage, map, rows, H.geom[op], pg, s);
+    } else {
+      if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
+      e = launch_retile(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], pg, s);
+    }
     return e == cudaSuccess ? MK_OK : cuda_code(e);
   };
 #define TRY(x)                  \

@@ -13,6 +13,7 @@ of this project:
   llama1b_b8_ragged    same shape, batch 8, per-sequence context U{128..4096}, 64 steps
   llama8b_ctx2048      32 layers, H 4096, 32 q / 8 kv heads of 128, FFN 14336,
                        vocab 128256, untied, theta 5e5, batch 1, context 2048, 64 steps
+  tiny_b4_ragged       the tiny shape at batch 4, per-sequence context U{16..64}, 8 steps
 
 Recipe (all seeded, counter-based, see synth.c):
   projection and embedding matrices  bf16(N(0, 0.02))
@@ -40,6 +41,8 @@ WORKLOADS = {
     "llama1b_ctx8192": dict(model=LLAMA1B, batch=1, ctx=8192, steps=64),
     "llama1b_b8_ragged": dict(model=LLAMA1B, batch=8, ctx=(128, 4096), steps=64),
     "llama8b_ctx2048": dict(model=LLAMA8B, batch=1, ctx=2048, steps=64),
+    # small batched parity case (the tensor-core projections of batch > 1)
+    "tiny_b4_ragged": dict(model=TINY, batch=4, ctx=(16, 64), steps=8),
 }
 ORDER = ["tiny", "llama1b_ctx1024", "llama1b_ctx8192", "llama1b_b8_ragged", "llama8b_ctx2048"]
 

@@ -70,6 +70,20 @@ def test_full_size_workloads(name, steps):
         s.close()
 
 
+@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC])
+def test_tiny_batched_tensor_core_path(sched):
+    """Batch > 1: every projection on tcgen05 (split along K, last slice
+    reduces), all steps teacher-forced against the oracle."""
+    s = Setup("tiny_b4_ragged", sched=sched)
+    try:
+        worst = teacher_forced(s, s.steps)
+        print("tiny_b4_ragged: worst max|d|=%.3g relL2=%.3g" % worst)
+        check_counters(s, s.steps)
+        kv_matches_oracle(s)
+    finally:
+        s.close()
+
+
 def test_static_schedule_full_size():
     s = Setup("llama1b_ctx1024", sched=mk.MK_SCHED_STATIC)
     try:
