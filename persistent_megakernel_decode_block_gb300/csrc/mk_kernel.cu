@@ -283,12 +283,12 @@ DEVI bool warp_wait(const KParams &P, const Smem &S, uint64_t *bar, uint32_t par
 }
 
 // ----------------------------------------------------- attention range ----
-// Chunk c of nch covers positions [p0, p1) of 0..pos: every chunk has the
-// same length (a multiple of 16), the last ones may be short or empty.
-DEVI void attn_range(int pos, int nch, int c, int &p0, int &p1) {
-  const int sb = (((pos + 1) + nch - 1) / nch + 15) & ~15;
-  p0 = c * sb;
-  p1 = min(p0 + sb, pos + 1);
+// Chunk c covers positions [c * attn_chunk, (c + 1) * attn_chunk) of 0..pos:
+// the chunks past p_b are empty (their instructions only take part in the
+// arrival), so a short sequence of a ragged batch costs few chunks.
+DEVI void attn_range(const KParams &P, int pos, int c, int &p0, int &p1) {
+  p0 = c * P.attn_chunk;
+  p1 = min(p0 + P.attn_chunk, pos + 1);
   if (p1 < p0) p1 = p0;
 }
 
@@ -301,7 +301,7 @@ DEVI uint32_t n_pages(const KParams &P, const Smem &S, const mk_instr &in) {
   if (in.op != MK_OP_ATTN) return in.npages;
   int p0, p1;
   const int pos = S.pos[in.b];
-  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  attn_range(P, pos, in.chunk, p0, p1);
   const int n_old = max(0, min(p1, pos) - p0);
   const int rpp = P.page_bytes / (P.d * 2);
   return 2u * (uint32_t)((n_old + rpp - 1) / rpp);
@@ -325,7 +325,7 @@ DEVI void page_src(const KParams &P, const Smem &S, const mk_instr &in, uint32_t
   }
   int p0, p1;
   const int pos = S.pos[in.b];
-  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  attn_range(P, pos, in.chunk, p0, p1);
   const int n_old = max(0, min(p1, pos) - p0);
   const int rpp = P.page_bytes / (P.d * 2);
   const uint32_t npk = np / 2;
@@ -978,7 +978,7 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   constexpr int DPL = D / 32;     // value dims per lane
   const int b = in.b, g = in.g, pos = S.pos[b];
   int p0, p1;
-  attn_range(pos, in.nchunk, in.chunk, p0, p1);
+  attn_range(P, pos, in.chunk, p0, p1);
   const int n_tot = p1 - p0;
   const int n_old = max(0, min(p1, pos) - p0);  // rows that come from the ring
   const uint32_t E = P.ring_pages;
@@ -989,6 +989,7 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   const int part = lane % LPP;
   const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
   SlotMeta &mw = const_cast<SlotMeta &>(meta);  // this entry's slot in shared memory
+  if (n_tot > 0) {  // (an empty chunk only takes part in the arrival)
 
   // query slice of head h (8 dims per lane), pre-scaled by 1/sqrt(d); the
   // current position's key slice and value dims if this warp covers p_b
@@ -1179,6 +1180,8 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
     }
   }
 
+  }  // n_tot > 0
+
   // 6. arrival: the chunk that completes its (sequence, group) merges all of
   //    the group's chunk partials by log-sum-exp, in chunk order, with every
   //    compute thread (one output each, eight chunks' loads in flight), and
@@ -1192,8 +1195,10 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   }
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
   if (S.misc[2]) {
-    const int PS = 2 * QPG + QPG * D, nch = (int)in.nchunk;
-    const float *pb = P.part + ((size_t)b * P.nkv + g) * nch * PS;
+    const int PS = 2 * QPG + QPG * D;
+    // chunks past p_b are empty and wrote nothing
+    const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
+    const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
     for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
       const int h = o / D;
       float M = -INFINITY, den = 0.f, num = 0.f;
