@@ -19,6 +19,7 @@ constexpr int kMaxItems = 256;  // work items (row x slice) per GEMV instruction
 constexpr int kMaxItemsB = 256; // work items x batch per GEMV instruction
 constexpr int kMaxChunks = 4;   // 256-column chunks per item: the input slice a lane keeps in
                                 // registers (8 per chunk); 4 keeps the GEMV loop free of spills
+constexpr int kTcBufs = 4;     // ring slots of the tensor-core B operand (one page's columns each)
 constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
 constexpr int kMaxRing = 32;
 // block flags (bail, bad input) at the start of the misc area, then the

@@ -187,6 +187,7 @@ DEVI float warp_max(float v) {
 struct Smem {
   uint8_t *ring;
   uint64_t *full, *empty, *ifull, *iempty, *rdy, *done, *attbar, *xbar, *tbar, *dbar;
+  uint64_t *bfull, *bempty;  // tensor-core B-operand slots written / read by the MMAs
   mk_instr *fifo;
   SlotMeta *meta;
   float *res, *opart, *ml, *sc, *rope, *normr, *rbuf, *xs;
@@ -212,6 +213,8 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.xbar = S.attbar + 1;
   S.tbar = S.xbar + 1;  // tensor-core results of a tile ready
   S.dbar = S.tbar + 1;  // every tensor-core operation drained (kernel end)
+  S.bfull = S.dbar + 1;
+  S.bempty = S.bfull + kTcBufs;
   S.fifo = reinterpret_cast<mk_instr *>(base + P.off_fifo);
   S.meta = reinterpret_cast<SlotMeta *>(base + P.off_meta);
   S.res = reinterpret_cast<float *>(base + P.off_res);
@@ -841,14 +844,16 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
 
 // One batch > 1 projection tile: MR weight rows x KS input columns (slice
 // `chunk` of `nchunk`), on the tensor cores.
-//  1. The compute warps stage the MMA's B operand: the slice of the B
-//     (normalised) input rows as bf16 values in rows 0..B-1 and as bf16
-//     remainders x - bf16(x) in rows B..2B-1, so value plus remainder keep
-//     about 16 significant bits of the fp32 input.
+//  1. The compute warps stage the MMA's B operand page by page into a ring
+//     of kTcBufs shared-memory slots, kTcBufs - 1 pages ahead of the MMAs:
+//     the page's columns of the B (normalised) input rows as bf16 values in
+//     rows 0..B-1 and as bf16 remainders x - bf16(x) in rows B..2B-1, so
+//     value plus remainder keep about 16 significant bits of the fp32 input.
+//     A slot is refilled once the commit of the MMAs that read it lands.
 //  2. Compute warp 0 lane 0 issues the MMAs (A = the ring page, K-major,
-//     fp32 accumulator in tensor memory) page by page as pages land; a commit
-//     releases each page once its MMAs are done (the other warps' arrivals
-//     make up the rest of the page's release count).
+//     fp32 accumulator in tensor memory) page by page as weight page and B
+//     slot land; a commit releases each page once its MMAs are done (the
+//     other warps' arrivals make up the rest of the page's release count).
 //  3. The four warps whose ids cover the four lane quarters of tensor memory
 //     read the MR x N accumulator and write value + remainder column, the
 //     tile's partial sums, to global memory.
@@ -857,9 +862,9 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
 __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_instr &in,
                                      const SlotMeta &meta, int cw, int lane, uint32_t epoch,
                                      uint32_t &xkey, uint32_t &xbar_uses, uint32_t &key_changes,
-                                     uint32_t &tc_uses) {
+                                     uint32_t &tc_uses, uint32_t &bseq) {
   const OpGeom &G = P.geom[in.op];
-  const int B = P.B, NB = P.tc_nb, MR = (int)G.MR, KS = (int)G.KS;
+  const int B = P.B, NB = P.tc_nb, MR = (int)G.MR, kc = (int)G.kc;
   const int tid = cw * 32 + lane;
   const uint32_t key = input_key(in);
   if (key != xkey) {
@@ -872,46 +877,64 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const uint16_t *gain = gain_of(P, in.op, in.layer);
   uint8_t *bop = reinterpret_cast<uint8_t *>(S.xs);
-  const int c0 = (int)in.chunk * KS;
-  // 1. B operand (rows >= 2B stay zero from the kernel's start)
-  for (int t = tid; t < B * (KS / 8); t += kComputeWarps * 32) {
-    const int b = t / (KS / 8), k = (t % (KS / 8)) * 8;
-    float v[8], g8[8];
-    load8(P, S, in.op, emb, b, c0 + k, v);
-    if (gain) load_gain8(gain, c0 + k, g8);
-    uint32_t hi[4], lo[4];
+  const uint32_t slot_bytes = (uint32_t)kc * (uint32_t)NB * 2u;
+  const int c0 = (int)in.chunk * (int)G.KS;
+  const uint32_t where = kWhereCompute | meta.idx, np = meta.npages, b0 = bseq;
+  // 1. B operand of page q (rows >= 2B stay zero from the kernel's start)
+  auto produce = [&](uint32_t q) -> bool {
+    const uint32_t n = b0 + q, bs = n % kTcBufs;
+    if (n >= (uint32_t)kTcBufs &&
+        !warp_wait(P, S, &S.bempty[bs], (n / kTcBufs - 1u) & 1u, where))
+      return false;
+    uint8_t *dst = bop + bs * slot_bytes;
+    const int cq = c0 + (int)q * kc;
+    for (int t = tid; t < B * (kc / 8); t += kComputeWarps * 32) {
+      const int b = t / (kc / 8), k = (t % (kc / 8)) * 8;
+      float v[8], g8[8];
+      load8(P, S, in.op, emb, b, cq + k, v);
+      if (gain) load_gain8(gain, cq + k, g8);
+      uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      const float x0 = v[u] * normr[b] * (gain ? g8[u] : 1.f);
-      const float x1 = v[u + 1] * normr[b] * (gain ? g8[u + 1] : 1.f);
-      const uint16_t h0 = to_bf(x0), h1 = to_bf(x1);
-      const uint16_t l0 = to_bf(x0 - bf1(h0)), l1 = to_bf(x1 - bf1(h1));
-      hi[u / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-      lo[u / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      for (int u = 0; u < 8; u += 2) {
+        const float x0 = v[u] * normr[b] * (gain ? g8[u] : 1.f);
+        const float x1 = v[u + 1] * normr[b] * (gain ? g8[u + 1] : 1.f);
+        const uint16_t h0 = to_bf(x0), h1 = to_bf(x1);
+        const uint16_t l0 = to_bf(x0 - bf1(h0)), l1 = to_bf(x1 - bf1(h1));
+        hi[u / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lo[u / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      }
+      const int kb = (k / 16) * (NB * 32) + ((k / 8) % 2) * 128;
+      *reinterpret_cast<uint4 *>(dst + kb + (b / 8) * 256 + (b % 8) * 16) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4 *>(dst + kb + ((B + b) / 8) * 256 + ((B + b) % 8) * 16) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    const int kb = (k / 16) * (NB * 32) + ((k / 8) % 2) * 128;
-    *reinterpret_cast<uint4 *>(bop + kb + (b / 8) * 256 + (b % 8) * 16) =
-        make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4 *>(bop + kb + ((B + b) / 8) * 256 + ((B + b) % 8) * 16) =
-        make_uint4(lo[0], lo[1], lo[2], lo[3]);
-  }
-  fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
-  if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+    fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.bfull[bs]);
+    return true;
+  };
+  for (uint32_t q = 0; q + 1 < (uint32_t)kTcBufs && q < np; ++q)
+    if (!produce(q)) return false;
   // 2. MMAs
   const uint32_t E = P.ring_pages, taddr = (uint32_t)S.misc[3];
-  const uint32_t idesc = tc_idesc((uint32_t)MR, (uint32_t)NB), bbase = saddr(bop);
-  if (cw == 0 && lane == 0) tc_fence_after();
-  for (uint32_t p = 0; p < meta.npages; ++p) {
+  const uint32_t idesc = tc_idesc((uint32_t)MR, (uint32_t)NB);
+  for (uint32_t p = 0; p < np; ++p) {
+    if (p + kTcBufs - 1 < np && !produce(p + kTcBufs - 1)) return false;
     const uint32_t seq = meta.seq0 + p, slot = seq % E;
-    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, kWhereCompute | meta.idx)) return false;
+    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, where)) return false;
     if (cw == 0) {
+      const uint32_t n = b0 + p, bs = n % kTcBufs;
+      if (!warp_wait(P, S, &S.bfull[bs], (n / kTcBufs) & 1u, where)) return false;
       if (lane == 0) {
+        tc_fence_after();
         const uint32_t abase = saddr(S.ring + (size_t)slot * P.page_bytes);
-        for (uint32_t t = 0; t < G.kc / 16; ++t)
+        const uint32_t bbase = saddr(bop + bs * slot_bytes);
+        for (uint32_t t = 0; t < (uint32_t)kc / 16; ++t)
           tc_mma(taddr, tc_desc(abase + t * (uint32_t)MR * 32, 128, 256),
-                 tc_desc(bbase + (p * (G.kc / 16) + t) * (uint32_t)NB * 32, 128, 256), idesc,
-                 (p | t) != 0);
+                 tc_desc(bbase + t * (uint32_t)NB * 32, 128, 256), idesc, (p | t) != 0);
         tc_commit(&S.empty[slot]);
+        tc_commit(&S.bempty[bs]);
       }
       __syncwarp();
     } else {
@@ -919,6 +942,7 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
       if (lane == 0) mbar_arrive(&S.empty[slot]);
     }
   }
+  bseq = b0 + np;
   if (cw == 0 && lane == 0) tc_commit(S.tbar);
   // 3. accumulator -> partial sums (warp w of the block reads lanes 32 (w % 4) ..)
   if (cw >= 2 && cw < 6) {
@@ -1318,7 +1342,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
 
 DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int lane) {
   uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu, tc_uses = 0;
-  uint32_t fs = 0;
+  uint32_t tc_bseq = 0, fs = 0;
   if (!next_entry(P, S, fs)) return;
   while (true) {
     const uint32_t f = fs % kFifo;
@@ -1338,7 +1362,8 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses, epoch);
       xkey = 0xFFFFFFFFu;
     } else {
-      ok = gemv_tc(P, S, in, meta, cw, lane, epoch, xkey, xbar_uses, key_changes, tc_uses);
+      ok = gemv_tc(P, S, in, meta, cw, lane, epoch, xkey, xbar_uses, key_changes, tc_uses,
+                   tc_bseq);
     }
     if (!ok) return;
     finish_entry(P, S, fs, cw, lane);
@@ -1501,6 +1526,10 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(S.xbar, kComputeWarps);
     mbar_init(S.tbar, 1);
     mbar_init(S.dbar, 1);
+    for (int i = 0; i < kTcBufs; ++i) {
+      mbar_init(&S.bfull[i], kComputeWarps);
+      mbar_init(&S.bempty[i], 1);
+    }
     fence_mbar_init();
     S.misc[0] = 0;
     S.misc[1] = 0;
@@ -1541,7 +1570,8 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t bop_bytes = 0;
     for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
-      if (op != MK_OP_ATTN) bop_bytes = max(bop_bytes, P.geom[op].KS * (uint32_t)P.tc_nb * 2u);
+      if (op != MK_OP_ATTN)
+        bop_bytes = max(bop_bytes, kTcBufs * P.geom[op].kc * (uint32_t)P.tc_nb * 2u);
     for (uint32_t i = tid; i < bop_bytes / 16; i += kThreads)
       reinterpret_cast<uint4 *>(S.xs)[i] = make_uint4(0u, 0u, 0u, 0u);
     tc_fence_before();

@@ -134,13 +134,18 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       g.kc = page / (g.MR * 2);
       if (g.kc < 16 || g.kc % 16) REJECT("page too small for a tensor-core tile");
       const uint32_t blocks = cdiv(rows_of[op], g.MR);
-      uint32_t ks = 512;
-      while (ks > g.kc && (g.K % ks || ks > g.K)) ks /= 2;
-      while (ks > g.kc && (uint64_t)blocks * (g.K / ks) < num_sms) ks /= 2;
-      if (ks % g.kc || g.K % ks) REJECT("input width does not split into tensor-core pages");
-      g.KS = ks;
-      g.S = g.K / ks;
-      g.ppt = ks / g.kc;
+      if (g.K % g.kc) REJECT("input width does not split into tensor-core pages");
+      // fewest slices (a divisor of the page count along K) that give the
+      // phase at least three tiles per four SMs
+      const uint32_t units = g.K / g.kc;
+      uint32_t nsl = 1;
+      while (nsl < units && (uint64_t)blocks * nsl * 4 < (uint64_t)num_sms * 3) {
+        ++nsl;
+        while (units % nsl) ++nsl;
+      }
+      g.S = nsl;
+      g.KS = g.K / nsl;
+      g.ppt = g.KS / g.kc;
       // outputs of each block (gate/up: MR/2 outputs = MR weight rows)
       const uint32_t per = op == MK_OP_GATEUP ? g.MR / 2 : g.MR;
       const uint32_t nout = op == MK_OP_QKV ? (uint32_t)GR : op == MK_OP_GATEUP ? (uint32_t)F
@@ -449,11 +454,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
   // staged GEMV input (normalised x, or the attention output) and attention scores
   uint32_t xs_floats = std::max<uint32_t>(H, QD);
-  if (P.tc)  // the MMA's B operand of one tile: KS x N bf16
+  if (P.tc)  // the MMA's B operand, one page's columns (kc x N bf16) per ring slot
     for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
-      if (op != MK_OP_ATTN) xs_floats = std::max<uint32_t>(xs_floats, P.geom[op].KS * P.tc_nb / 2);
+      if (op != MK_OP_ATTN)
+        xs_floats = std::max<uint32_t>(xs_floats, kTcBufs * P.geom[op].kc * P.tc_nb / 2);
   uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
-  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4) * 8;
+  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4 + 2 * kTcBufs) * 8;
   uint32_t rel_bars = take(bars_max, 8);
   uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
   uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);
