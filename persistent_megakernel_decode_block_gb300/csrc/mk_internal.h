@@ -39,10 +39,11 @@ constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2;
 // per lane.
 struct OpGeom {
   uint32_t K, NS, SW, item_bytes, ipp, nch;
-  // batch > 1 (tensor-core) plans: tiles of MR weight rows x KS input
-  // columns (S = K / KS slices per block of rows), pages of MR rows x kc
-  // columns in the MMA's core-matrix order, ppt pages per tile
-  uint32_t MR, KS, S, kc, ppt;
+  // batch > 1 (tensor-core) plans: blocks of MR weight rows stored as kp
+  // pages of MR rows x kc columns in the MMA's core-matrix order; a block is
+  // split along K into S slices of whole pages (slice s: pages
+  // [s kp / S, (s + 1) kp / S))
+  uint32_t MR, S, kc, kp;
 };
 
 struct KParams {

@@ -699,12 +699,41 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
   for (int b = cw; b < P.B; b += kComputeWarps) {  // a warp per sequence
     float r = 1.f;
     if (norm) {
+      // normalised inputs are x or an embedding row: 16 values of a lane in
+      // flight per round trip
       float ss = 0.f;
-      for (uint32_t c = lane * 8; c < G.K; c += 256) {
-        float v[8];
-        load8(P, S, in.op, emb, b, c, v);
+      if (emb) {
+        const uint16_t *row = P.embed + (size_t)S.tok[b] * P.H;
+        for (uint32_t c = lane * 8; c < G.K; c += 512) {
+          const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(row + c));
+          const uint4 w1 = c + 256 < G.K ? __ldg(reinterpret_cast<const uint4 *>(row + c + 256))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) ss = fmaf(v[t], v[t], ss);
+          for (int t = 0; t < 8; ++t) {
+            const float lo = bf_lo(w[t]), hi = bf_hi(w[t]);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+          }
+        }
+      } else {
+        const float *row = P.x + (size_t)b * P.H;
+        for (uint32_t c = lane * 8; c < G.K; c += 512) {
+          const bool two = c + 256 < G.K;
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 a0 = __ldcg(reinterpret_cast<const float4 *>(row + c));
+          const float4 a1 = __ldcg(reinterpret_cast<const float4 *>(row + c + 4));
+          const float4 a2 = two ? __ldcg(reinterpret_cast<const float4 *>(row + c + 256)) : z;
+          const float4 a3 = two ? __ldcg(reinterpret_cast<const float4 *>(row + c + 260)) : z;
+          const float4 q[4] = {a0, a1, a2, a3};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            ss = fmaf(q[t].x, q[t].x, ss);
+            ss = fmaf(q[t].y, q[t].y, ss);
+            ss = fmaf(q[t].z, q[t].z, ss);
+            ss = fmaf(q[t].w, q[t].w, ss);
+          }
+        }
       }
       ss = warp_sum(ss);
       r = rsqrtf(ss / (float)G.K + P.eps);
@@ -826,10 +855,10 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
         P.x[(size_t)b * P.H + row] = resid + val(r, b);
       }
       break;
-    case MK_OP_GATEUP:
+    case MK_OP_GATEUP:  // rows interleave gate j (2j) and up j (2j + 1)
       for (int u = tid; u < (int)in.nrows * B; u += T) {
         const int j = u % in.nrows, b = u / in.nrows;
-        const float gt = val(j, b), up = val(MR / 2 + j, b);
+        const float gt = val(2 * j, b), up = val(2 * j + 1, b);
         P.h[(size_t)b * P.F + in.row0 + j] = gt / (1.f + __expf(-gt)) * up;
       }
       break;
@@ -842,10 +871,10 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
   }
 }
 
-// One batch > 1 projection tile: MR weight rows x KS input columns (slice
-// `chunk` of `nchunk`), on the tensor cores.
-//  1. The compute warps stage the MMA's B operand page by page into a ring
-//     of kTcBufs shared-memory slots, kTcBufs - 1 pages ahead of the MMAs:
+// One batch > 1 projection tile: MR weight rows x the input columns of
+// slice `chunk` of `nchunk` (whole pages of kc columns), on the tensor cores.
+//  1. Compute warps 1.. stage the MMA's B operand page by page into a ring
+//     of kTcBufs shared-memory slots, kTcBufs - 2 pages ahead of the MMAs:
 //     the page's columns of the B (normalised) input rows as bf16 values in
 //     rows 0..B-1 and as bf16 remainders x - bf16(x) in rows B..2B-1, so
 //     value plus remainder keep about 16 significant bits of the fp32 input.
@@ -855,10 +884,13 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
 //     slot land; a commit releases each page once its MMAs are done (the
 //     other warps' arrivals make up the rest of the page's release count).
 //  3. The four warps whose ids cover the four lane quarters of tensor memory
-//     read the MR x N accumulator and write value + remainder column, the
-//     tile's partial sums, to global memory.
-//  4. The slice that completes its block (acq_rel arrival) runs tc_epilogue
-//     with every compute thread and releases the phase counter.
+//     read the MR x N accumulator and add value and remainder columns: an
+//     unsplit LM-head or gate/up tile writes its logits or SiLU(gate) * up
+//     from there; other tiles write these partial sums to global memory.
+//  4. An unsplit tile that wrote partial sums runs tc_epilogue itself; a
+//     split tile arrives on its block's counter (acq_rel) and the last slice
+//     runs tc_epilogue over the slices' sums.  Either releases the phase
+//     counter.
 __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_instr &in,
                                      const SlotMeta &meta, int cw, int lane, uint32_t epoch,
                                      uint32_t &xkey, uint32_t &xbar_uses, uint32_t &key_changes,
@@ -878,54 +910,77 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   const uint16_t *gain = gain_of(P, in.op, in.layer);
   uint8_t *bop = reinterpret_cast<uint8_t *>(S.xs);
   const uint32_t slot_bytes = (uint32_t)kc * (uint32_t)NB * 2u;
-  const int c0 = (int)in.chunk * (int)G.KS;
+  const int c0 = in.nchunk > 1 ? (int)(in.chunk * G.kp / in.nchunk) * kc : 0;
   const uint32_t where = kWhereCompute | meta.idx, np = meta.npages, b0 = bseq;
-  // 1. B operand of page q (rows >= 2B stay zero from the kernel's start)
-  auto produce = [&](uint32_t q) -> bool {
+  // 1. B operand of page q (rows >= 2B stay zero from the kernel's start),
+  //    written by compute warps 1.. (warp 0 issues the MMAs).  The producer
+  //    threads form NG groups of one (sequence, 8 columns) unit each; group
+  //    g owns pages g, g + NG, ... and fetches its next page's activations
+  //    right after storing one, so each fetch has NG pages' time to land.
+  //    Every producer warp arrives on every slot (after the wait for the
+  //    slot's previous MMAs), so a slot's count never depends on ownership.
+  const int units = B * (kc / 8), pt = tid - 32;
+  const int NG = ((kComputeWarps - 1) * 32) / units;  // >= 1 (checked by the planner)
+  const int grp = pt >= 0 ? pt / units : NG;
+  const bool has = grp < NG;
+  const int ub = has ? (pt % units) / (kc / 8) : 0, uk = has ? (pt % (kc / 8)) * 8 : 0;
+  float v[8];
+  auto fetch = [&](uint32_t q) {
+    if (has && q < np) load8(P, S, in.op, emb, ub, c0 + (int)q * kc + uk, v);
+  };
+  auto store = [&](uint32_t q) -> bool {
     const uint32_t n = b0 + q, bs = n % kTcBufs;
     if (n >= (uint32_t)kTcBufs &&
         !warp_wait(P, S, &S.bempty[bs], (n / kTcBufs - 1u) & 1u, where))
       return false;
-    uint8_t *dst = bop + bs * slot_bytes;
-    const int cq = c0 + (int)q * kc;
-    for (int t = tid; t < B * (kc / 8); t += kComputeWarps * 32) {
-      const int b = t / (kc / 8), k = (t % (kc / 8)) * 8;
-      float v[8], g8[8];
-      load8(P, S, in.op, emb, b, cq + k, v);
-      if (gain) load_gain8(gain, cq + k, g8);
+    if (has && (int)(q % (uint32_t)NG) == grp) {
+      uint8_t *dst = bop + bs * slot_bytes;
+      const float r = normr[ub];
+      float g8[8];
+      if (gain) load_gain8(gain, c0 + (int)q * kc + uk, g8);
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int u = 0; u < 8; u += 2) {
-        const float x0 = v[u] * normr[b] * (gain ? g8[u] : 1.f);
-        const float x1 = v[u + 1] * normr[b] * (gain ? g8[u + 1] : 1.f);
+        const float x0 = v[u] * r * (gain ? g8[u] : 1.f);
+        const float x1 = v[u + 1] * r * (gain ? g8[u + 1] : 1.f);
         const uint16_t h0 = to_bf(x0), h1 = to_bf(x1);
         const uint16_t l0 = to_bf(x0 - bf1(h0)), l1 = to_bf(x1 - bf1(h1));
         hi[u / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
         lo[u / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
       }
-      const int kb = (k / 16) * (NB * 32) + ((k / 8) % 2) * 128;
-      *reinterpret_cast<uint4 *>(dst + kb + (b / 8) * 256 + (b % 8) * 16) =
+      const int kb = (uk / 16) * (NB * 32) + ((uk / 8) % 2) * 128;
+      *reinterpret_cast<uint4 *>(dst + kb + (ub / 8) * 256 + (ub % 8) * 16) =
           make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4 *>(dst + kb + ((B + b) / 8) * 256 + ((B + b) % 8) * 16) =
+      *reinterpret_cast<uint4 *>(dst + kb + ((B + ub) / 8) * 256 + ((B + ub) % 8) * 16) =
           make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      fetch(q + (uint32_t)NG);
     }
     fence_proxy_async();  // generic-proxy writes become visible to the tensor cores
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.bfull[bs]);
     return true;
   };
-  for (uint32_t q = 0; q + 1 < (uint32_t)kTcBufs && q < np; ++q)
-    if (!produce(q)) return false;
-  // 2. MMAs
-  const uint32_t E = P.ring_pages, taddr = (uint32_t)S.misc[3];
-  const uint32_t idesc = tc_idesc((uint32_t)MR, (uint32_t)NB);
-  for (uint32_t p = 0; p < np; ++p) {
-    if (p + kTcBufs - 1 < np && !produce(p + kTcBufs - 1)) return false;
-    const uint32_t seq = meta.seq0 + p, slot = seq % E;
-    if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, where)) return false;
-    if (cw == 0) {
+  if (cw != 0) {
+    // 2a. producers: every page's slot, in order (at most kTcBufs ahead of
+    //     the MMAs through the slots' release)
+    fetch((uint32_t)grp);
+    for (uint32_t q = 0; q < np; ++q)
+      if (!store(q)) return false;
+  } else {
+    // 2b. MMAs: page p once its weights and its B slot are in; the commit
+    //     releases both (the page's only release in tensor-core plans)
+    const uint32_t E = P.ring_pages, taddr = (uint32_t)S.misc[3];
+    const uint32_t idesc = tc_idesc((uint32_t)MR, (uint32_t)NB);
+    const bool stamp = lane == 0 && (P.flags & MK_FLAG_TRACE);
+    SlotMeta &mw = const_cast<SlotMeta &>(meta);  // this entry's slot in shared memory
+    if (stamp) mw.t_input = gtimer();
+    for (uint32_t p = 0; p < np; ++p) {
+      const uint32_t seq = meta.seq0 + p, slot = seq % E;
       const uint32_t n = b0 + p, bs = n % kTcBufs;
+      if (!warp_wait(P, S, &S.full[slot], (seq / E) & 1u, where)) return false;
+      if (stamp && p == 0) mw.t_page0 = gtimer();
       if (!warp_wait(P, S, &S.bfull[bs], (n / kTcBufs) & 1u, where)) return false;
+      if (stamp && p + 1 == np) mw.t_pagel = gtimer();
       if (lane == 0) {
         tc_fence_after();
         const uint32_t abase = saddr(S.ring + (size_t)slot * P.page_bytes);
@@ -937,12 +992,14 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
         tc_commit(&S.bempty[bs]);
       }
       __syncwarp();
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
     }
   }
   bseq = b0 + np;
+  const uint32_t taddr = (uint32_t)S.misc[3];
+  // an unsplit LM-head or gate/up tile writes its outputs straight from the
+  // accumulator; other tiles go through the partial-sum buffer
+  const bool unsplit = in.sig2_ctr == MK_NO_COUNTER;
+  const bool direct = unsplit && (in.op == MK_OP_LMHEAD || in.op == MK_OP_GATEUP);
   if (cw == 0 && lane == 0) tc_commit(S.tbar);
   // 3. accumulator -> partial sums (warp w of the block reads lanes 32 (w % 4) ..)
   if (cw >= 2 && cw < 6) {
@@ -956,17 +1013,42 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
       const uint32_t ta = taddr + ((uint32_t)(32 * qd) << 16);
       tc_ld16(ta, v0);
       if (NB > 16) tc_ld16(ta + 16, v1);
-      const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
       const int r = 32 * qd + lane;
-      float *dst = P.gpart + (((size_t)rb * in.nchunk + in.chunk) * MR + r) * B;
+      if (direct && in.op == MK_OP_LMHEAD) {
+        if (r < (int)in.nrows)
 #pragma unroll
-      for (int b = 0; b < kMaxBatch; ++b)
-        if (b < B) dst[b] = v[b] + v[B + b];
+          for (int b = 0; b < kMaxBatch; ++b)
+            if (b < B) P.logits[(size_t)b * P.V + in.row0 + r] = v[b] + v[B + b];
+      } else if (direct) {  // gate/up: lane 2j holds gate j, lane 2j + 1 up j
+        const int j = r / 2;
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b)
+          if (b < B) {
+            const float x = v[b] + v[B + b];
+            const float up = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+            if (!(lane & 1) && j < (int)in.nrows)
+              P.h[(size_t)b * P.F + in.row0 + j] = x / (1.f + __expf(-x)) * up;
+          }
+      } else {
+        const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
+        float *dst = P.gpart + (((size_t)rb * in.nchunk + in.chunk) * MR + r) * B;
+#pragma unroll
+        for (int b = 0; b < kMaxBatch; ++b)
+          if (b < B) dst[b] = v[b] + v[B + b];
+      }
     }
   }
   ++tc_uses;
   tc_fence_before();
   if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+  if (unsplit) {  // the tile owns its rows: finish them and signal the phase
+    if (!direct) {
+      tc_epilogue(P, S, in, tid);
+      if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+    }
+    if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
+    return true;
+  }
   // 4. arrival; the block's last slice sums the slices and finishes the rows
   if (cw == 0 && lane == 0) {
     const uint32_t old = atom_add_acq_rel(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
@@ -1044,7 +1126,6 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   const uint8_t *__restrict__ vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
   if (paged && !warp_wait(P, S, &S.full[meta.seq0 % E], (meta.seq0 / E) & 1u, kWhereCompute | meta.idx))
     return false;
-  if (stamp) mw.t_page0 = gtimer();
 
   // 1. scores of rows j0..j1 into this warp's row of S.sc.  A block of LPP
   //    steps covers 32 rows; each lane keeps its LPP partial dot products and
@@ -1089,6 +1170,7 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
     if (jr < j1) sw[jr - j0] = v[0];
   }
   __syncwarp();
+  if (stamp) mw.t_page0 = gtimer();
 
   // 2. this warp's maximum, probabilities and denominator
   const int cnt = j1 - j0;
@@ -1108,6 +1190,7 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   if (paged && !warp_wait(P, S, &S.full[(meta.seq0 + 1) % E], ((meta.seq0 + 1) / E) & 1u,
                           kWhereCompute | meta.idx))
     return false;
+  if (stamp) mw.t_pagel = gtimer();
   float o[8][DPL];
 #pragma unroll
   for (int u = 0; u < 8; ++u)
@@ -1156,11 +1239,10 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   }
   // every warp is done with the chunk's pages
   __syncwarp();
-  if (paged && lane == 0) {
+  if (paged && !P.tc && lane == 0) {
     mbar_arrive(&S.empty[meta.seq0 % E]);
     mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
   }
-  if (stamp) mw.t_pagel = gtimer();
 
   // 4. per-warp partials (double-buffered by instruction parity: a warp can
   //    be at most one instruction ahead of the warps merging the last one)
@@ -1176,6 +1258,10 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
     mlp[cw * 2 + 1] = l;
   }
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (paged && P.tc && cw == 0 && lane == 0) {  // every warp is past the pages
+    mbar_arrive(&S.empty[meta.seq0 % E]);
+    mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
+  }
 
   // 5. warp hh < QPG merges the partials of head hh into the chunk partial
   if (cw < QPG) {
@@ -1340,6 +1426,11 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
   }
 }
 
+// The compute warps' loop.  Batch-1 plans run every projection as a CUDA-core
+// GEMV; batch > 1 plans run them on the tensor cores.  The two are separate
+// instantiations (and kernels), so neither's registers are shaped by the
+// other's calls.
+template <bool TC>
 DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int lane) {
   uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu, tc_uses = 0;
   uint32_t tc_bseq = 0, fs = 0;
@@ -1352,7 +1443,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       finish_entry(P, S, fs, cw, lane);
       return;
     }
-    if (in.op != MK_OP_ATTN && P.B == 1) {
+    if (!TC && in.op != MK_OP_ATTN) {
       if (!run_gemv_b1(P, S, fs, epoch, cw, lane, xbar_uses)) return;
       continue;
     }
@@ -1361,9 +1452,11 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
     if (in.op == MK_OP_ATTN) {
       ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses, epoch);
       xkey = 0xFFFFFFFFu;
-    } else {
+    } else if (TC) {
       ok = gemv_tc(P, S, in, meta, cw, lane, epoch, xkey, xbar_uses, key_changes, tc_uses,
                    tc_bseq);
+    } else {
+      ok = false;
     }
     if (!ok) return;
     finish_entry(P, S, fs, cw, lane);
@@ -1500,8 +1593,8 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
 }
 
 // --------------------------------------------------------------- kernel ----
-extern "C" __global__ void __launch_bounds__(kThreads, 1)
-    mk_megakernel(const __grid_constant__ KParams P) {
+template <bool TC>
+DEVI void megakernel_body(const KParams &P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // The table of shared-memory pointers lives in shared memory itself: a
@@ -1514,7 +1607,9 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (uint32_t i = 0; i < P.ring_pages; ++i) {
       mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], kComputeWarps);
+      // tensor-core plans: a page's one release is the MMA commit (a
+      // projection) or compute warp 0 after the block's barrier (attention)
+      mbar_init(&S.empty[i], P.tc ? 1 : kComputeWarps);
     }
     for (int i = 0; i < kFifo; ++i) {
       mbar_init(&S.ifull[i], 1);
@@ -1527,7 +1622,7 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(S.tbar, 1);
     mbar_init(S.dbar, 1);
     for (int i = 0; i < kTcBufs; ++i) {
-      mbar_init(&S.bfull[i], kComputeWarps);
+      mbar_init(&S.bfull[i], kComputeWarps - 1);
       mbar_init(&S.bempty[i], 1);
     }
     fence_mbar_init();
@@ -1559,7 +1654,7 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0 && blockIdx.x == 0) raise_error(P, MK_ERR_BOUNDS, 0, false);
     return;
   }
-  if (P.tc) {
+  if (TC) {
     // tensor memory for the projections' accumulator (at most 32 fp32
     // columns), and a zeroed B-operand buffer (rows past 2B stay zero)
     if (warp == 2) {
@@ -1584,10 +1679,10 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     storer(P, S, epoch, lane);
   } else {
-    compute(P, S, epoch, warp - 2, lane);
+    compute<TC>(P, S, epoch, warp - 2, lane);
   }
   __syncthreads();
-  if (P.tc) {
+  if (TC) {
     // every tensor-core operation (issued by compute warp 0 lane 0) is done
     // before the accumulator's tensor memory is freed
     if (warp == 2 && lane == 0) {
@@ -1613,6 +1708,17 @@ extern "C" __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t old = atomicAdd(P.ctrl + kCtlExit, 1u);
     if (old == epoch * P.n_blocks + P.n_blocks - 1u) atomicExch(P.ctrl + kCtlEpoch, epoch + 1u);
   }
+}
+
+// Batch-1 plans (CUDA-core GEMVs) and batch > 1 plans (tensor-core
+// projections): the same persistent interpreter, compiled twice.
+extern "C" __global__ void __launch_bounds__(kThreads, 1)
+    mk_megakernel(const __grid_constant__ KParams P) {
+  megakernel_body<false>(P);
+}
+extern "C" __global__ void __launch_bounds__(kThreads, 1)
+    mk_megakernel_tc(const __grid_constant__ KParams P) {
+  megakernel_body<true>(P);
 }
 
 // The multi-kernel path ends each step with this one-thread launch.
@@ -1644,23 +1750,23 @@ extern "C" __global__ void mk_retile(uint8_t *dst, const uint8_t *src, const int
   }
 }
 
-// Tensor-core tiles (batch > 1 plans): weight row k (source row map[k]) and
-// 8 columns from c go to block rb = k / MR (row rr = k % MR), slice c / KS,
-// page (c % KS) / kc of the slice, and inside the page to the core matrix
+// Tensor-core blocks (batch > 1 plans): weight row k (source row map[k]) and
+// 8 columns from c go to block rb = k / MR (row rr = k % MR), page c / kc of
+// the block's kp pages along K, and inside the page to the core matrix
 // (rr / 8, (cc / 8) % 2) of k-step cc / 16, cc = c % kc: the MMA reads a
 // k-step as MR x 16 bf16 in 8-row x 16-byte core matrices, 128 bytes apart
 // along K and 256 bytes apart along M.
 extern "C" __global__ void mk_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *map,
-                                        uint32_t nrows, uint32_t K, uint32_t MR, uint32_t KS,
-                                        uint32_t S, uint32_t kc, uint32_t ppt, uint32_t page) {
+                                        uint32_t nrows, uint32_t K, uint32_t MR, uint32_t kc,
+                                        uint32_t kp, uint32_t page) {
   const uint64_t per_row = K / 8;
   const uint64_t total = (uint64_t)nrows * per_row;
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (uint64_t)gridDim.x * blockDim.x) {
     const uint32_t k = (uint32_t)(i / per_row);
     const uint32_t c = (uint32_t)(i % per_row) * 8;
-    const uint32_t rb = k / MR, rr = k % MR, sl = c / KS, j = (c % KS) / kc, cc = c % kc;
-    uint8_t *d = dst + (((uint64_t)rb * S + sl) * ppt + j) * page + (cc / 16) * (MR * 32) +
+    const uint32_t rb = k / MR, rr = k % MR, j = c / kc, cc = c % kc;
+    uint8_t *d = dst + ((uint64_t)rb * kp + j) * page + (cc / 16) * (MR * 32) +
                  (rr / 8) * 256 + ((cc / 8) % 2) * 128 + (rr % 8) * 16;
     const uint32_t srow = map ? (uint32_t)map[k] : k;
     *reinterpret_cast<uint4 *>(d) =
@@ -1670,6 +1776,9 @@ extern "C" __global__ void mk_retile_tc(uint8_t *dst, const uint8_t *src, const 
 
 // ---- host-side launch helpers (the kernels' host stubs live in this unit) ----
 cudaError_t set_megakernel_smem(uint32_t bytes) {
+  const cudaError_t e = cudaFuncSetAttribute(mk_megakernel_tc,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)bytes);
 }
@@ -1686,7 +1795,8 @@ cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cooperative ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, mk_megakernel, P);
+  return P.tc ? cudaLaunchKernelEx(&cfg, mk_megakernel_tc, P)
+              : cudaLaunchKernelEx(&cfg, mk_megakernel, P);
 }
 
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream) {
@@ -1698,8 +1808,8 @@ cudaError_t launch_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *ma
                              uint32_t nrows, const OpGeom &g, uint32_t page, cudaStream_t stream) {
   const uint64_t total = (uint64_t)nrows * g.K / 8;
   const uint32_t blocks = (uint32_t)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
-  mk_retile_tc<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, nrows, g.K, g.MR, g.KS, g.S,
-                                                         g.kc, g.ppt, page);
+  mk_retile_tc<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, nrows, g.K, g.MR, g.kc,
+                                                         g.kp, page);
   return cudaGetLastError();
 }
 

@@ -119,9 +119,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   if (too_big && B == 1) REJECT("a GEMV tile has too many items");
   // Batch > 1: every projection runs on the tensor cores (tcgen05, M = MR
   // weight rows, N = the batch's values and bf16 remainders).  A block of MR
-  // rows is split along K into S slices of KS columns so that a phase has at
-  // least as many tiles as SMs; the last slice of a block to finish sums the
-  // slices (in slice order) and applies the epilogue.
+  // rows is split along K into S slices of whole pages, as many as keep the
+  // phase within one tile per SM; the last slice of a block to finish sums
+  // the slices (in slice order) and applies the epilogue.
   P.tc = B > 1;
   if (P.tc) {
     P.tc_nb = 16 * cdiv(2 * (uint32_t)B, 16);
@@ -133,19 +133,14 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       g.MR = (op == MK_OP_QKV && GR % 128) ? 64 : 128;
       g.kc = page / (g.MR * 2);
       if (g.kc < 16 || g.kc % 16) REJECT("page too small for a tensor-core tile");
+      if ((uint32_t)B * (g.kc / 8) > (kComputeWarps - 1) * 32u)
+        REJECT("batch too large for the page size on the tensor-core path");
       const uint32_t blocks = cdiv(rows_of[op], g.MR);
       if (g.K % g.kc) REJECT("input width does not split into tensor-core pages");
-      // fewest slices (a divisor of the page count along K) that give the
-      // phase at least three tiles per four SMs
-      const uint32_t units = g.K / g.kc;
-      uint32_t nsl = 1;
-      while (nsl < units && (uint64_t)blocks * nsl * 4 < (uint64_t)num_sms * 3) {
-        ++nsl;
-        while (units % nsl) ++nsl;
-      }
-      g.S = nsl;
-      g.KS = g.K / nsl;
-      g.ppt = g.KS / g.kc;
+      // as many slices as keep the phase within one tile per SM (slice s
+      // takes pages [s kp / S, (s + 1) kp / S) along K)
+      g.kp = g.K / g.kc;
+      g.S = std::max<uint32_t>(1, std::min<uint32_t>(g.kp, num_sms / blocks));
       // outputs of each block (gate/up: MR/2 outputs = MR weight rows)
       const uint32_t per = op == MK_OP_GATEUP ? g.MR / 2 : g.MR;
       const uint32_t nout = op == MK_OP_QKV ? (uint32_t)GR : op == MK_OP_GATEUP ? (uint32_t)F
@@ -158,7 +153,6 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   }
   auto wrows_of = [](int op, uint32_t n) { return op == MK_OP_GATEUP ? 2 * n : n; };
   auto tile_pages = [&](int op, uint32_t wrows) {
-    if (P.tc) return P.geom[op].ppt;
     return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp);
   };
   uint32_t tile_items_max = 0;
@@ -176,8 +170,8 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     for (int g = 0; g < reps; ++g)
       for (uint32_t n : P.tiles[op]) {
         const uint32_t w = wrows_of(op, n);
-        if (P.tc) {  // tensor-core tiles: S slices of ppt pages; retiled by formula
-          toff += (uint64_t)P.geom[op].S * P.geom[op].ppt * page;
+        if (P.tc) {  // tensor-core blocks: kp pages along K; retiled by formula
+          toff += (uint64_t)P.geom[op].kp * page;
           continue;
         }
         for (uint32_t r = 0; r < w; ++r) rt.push_back(toff | r);
@@ -278,6 +272,16 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       P.ctr_inc[in.sig_ctr]++;
       return;
     }
+    if (g.S == 1) {  // unsplit: the tile finishes its rows and signals the phase
+      in.chunk = 0;
+      in.nchunk = 1;
+      in.npages = g.kp;
+      in.wofs = off;
+      off += (uint64_t)in.npages * page;
+      push(in);
+      P.ctr_inc[in.sig_ctr]++;
+      return;
+    }
     const uint32_t phase_ctr = in.sig_ctr, arr = next_arr++;
     for (uint32_t sl = 0; sl < g.S; ++sl) {
       mk_instr t = in;
@@ -286,9 +290,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
       t.sig2_after = g.S;
       t.chunk = sl;
       t.nchunk = g.S;
-      t.npages = g.ppt;
+      t.npages = (sl + 1) * g.kp / g.S - sl * g.kp / g.S;
       t.wofs = off;
-      off += (uint64_t)g.ppt * page;
+      off += (uint64_t)t.npages * page;
       push(t);
       P.ctr_inc[arr]++;
     }
@@ -422,8 +426,15 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     size_t k = 0;
     uint32_t r0 = 0;
     for (uint32_t nr : P.tiles[MK_OP_GATEUP]) {
-      for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(r0 + j);
-      for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(F + r0 + j);
+      if (P.tc) {  // tensor-core tiles interleave: row 2j gate j, row 2j + 1 up j
+        for (uint32_t j = 0; j < nr; ++j) {
+          P.gu_map[k++] = (int32_t)(r0 + j);
+          P.gu_map[k++] = (int32_t)(F + r0 + j);
+        }
+      } else {  // GEMV tiles: the tile's gate rows, then its up rows
+        for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(r0 + j);
+        for (uint32_t j = 0; j < nr; ++j) P.gu_map[k++] = (int32_t)(F + r0 + j);
+      }
       r0 += nr;
     }
   }
