@@ -100,6 +100,31 @@ def test_tables_are_deterministic():
         mk.mk_destroy(b)
 
 
+@pytest.mark.parametrize("name", [n for n in ORDER if WORKLOADS[n]["batch"] > 1])
+def test_tensor_core_tiles_split_along_k_in_whole_balanced_slices(name):
+    """Batch > 1 projection tiles: every tile names its slice (chunk < nchunk,
+    nchunk >= 1, also when unsplit), a split block has slices 0..S-1 sharing
+    one arrival counter, with page counts that differ by at most one."""
+    p = host_plan(name)
+    try:
+        rec, _, _ = mk.mk_plan_tables(p)
+        proj = rec[rec["op"] != mk.MK_OP_ATTN]
+        proj = proj[(proj["op"] >= mk.MK_OP_QKV) & (proj["op"] <= mk.MK_OP_LMHEAD)]
+        assert len(proj)
+        assert (proj["nchunk"] >= 1).all() and (proj["chunk"] < proj["nchunk"]).all()
+        unsplit = proj["sig2_ctr"] == mk.MK_NO_COUNTER
+        assert (proj["nchunk"][unsplit] == 1).all()
+        split = proj[~unsplit]
+        for ctr in np.unique(split["sig_ctr"]):
+            blk = split[split["sig_ctr"] == ctr]
+            S = int(blk["nchunk"][0])
+            assert sorted(blk["chunk"].tolist()) == list(range(S))
+            assert (blk["sig2_after"] == S).all() and len(np.unique(blk["sig2_ctr"])) == 1
+            assert blk["npages"].max() - blk["npages"].min() <= 1
+    finally:
+        mk.mk_destroy(p)
+
+
 def test_fault_flag_makes_one_target_unreachable():
     w = WORKLOADS["tiny"]
     p = host_plan("tiny", flags=mk.MK_FLAG_FAULT_WAIT)
