@@ -1095,7 +1095,9 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   const int part = lane % LPP;
   const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
   SlotMeta &mw = const_cast<SlotMeta &>(meta);  // this entry's slot in shared memory
-  if (n_tot > 0) {  // (an empty chunk only takes part in the arrival)
+  // A chunk past p_b has nothing to do: it neither computes nor arrives (the
+  // group's last real chunk adds the empty chunks' share of the arrivals).
+  if (n_tot <= 0) return true;
 
   // query slice of head h (8 dims per lane), pre-scaled by 1/sqrt(d); the
   // current position's key slice and value dims if this warp covers p_b
@@ -1290,24 +1292,27 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
     }
   }
 
-  }  // n_tot > 0
-
   // 6. arrival: the chunk that completes its (sequence, group) merges all of
   //    the group's chunk partials by log-sum-exp, in chunk order, with every
   //    compute thread (one output each, eight chunks' loads in flight), and
   //    releases the group counter.  The acq_rel arrival publishes this chunk's
   //    partial (ordered before it by the barrier) and, for the last arriver,
   //    acquires every other chunk's.
+  //    Only the nch chunks that reach p_b arrive: the last of them also adds
+  //    the nchunk - nch empty chunks' share, so the counter still advances by
+  //    nchunk per step.
+  const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
   if (cw == 0 && lane == 0) {
-    const uint32_t old = atom_add_acq_rel(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
-    S.misc[2] = old == epoch * in.nchunk + in.nchunk - 1u ? 1 : 0;
+    uint32_t *ctr = P.ctr + (size_t)in.sig_ctr * kCtrStride;
+    const uint32_t old = atom_add_acq_rel(ctr, 1u);
+    const bool last = old == epoch * in.nchunk + (uint32_t)nch - 1u;
+    if (last && (uint32_t)nch < in.nchunk) red_add(ctr, in.nchunk - (uint32_t)nch);
+    S.misc[2] = last ? 1 : 0;
   }
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
   if (S.misc[2]) {
     const int PS = 2 * QPG + QPG * D;
-    // chunks past p_b are empty and wrote nothing
-    const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
     const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
     for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
       const int h = o / D;
