@@ -76,7 +76,8 @@ def kernel_sha256():
 def recorded_traffic(workload):
     """dram bytes read + written per launch from the committed ncu summary of
     this workload, or None when the kernel changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "mk_megakernel_%s_sections.md" % workload)
+    kernel = "mk_megakernel_tc" if WORKLOADS[workload]["batch"] > 1 else "mk_megakernel"
+    path = os.path.join(ROOT, "profiles", "%s_%s_sections.md" % (kernel, workload))
     try:
         kv = {}
         for line in open(path):
