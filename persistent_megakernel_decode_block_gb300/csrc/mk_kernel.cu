@@ -374,6 +374,50 @@ DEVI void load_record(const KParams &P, uint32_t idx, uint4 (&r)[4]) {
   }
 }
 
+// Static lists and ragged batches: whether an attention chunk has work
+// depends on its sequence's position, known only at run time, so a fixed
+// round-robin of chunk instructions can hand one SM six chunks with work and
+// another two.  Instead the list slots of a layer's attention phase are
+// re-dealt at run time, identically on every SM: slot j (phase order: chunk,
+// sequence, group) takes the j-th instruction of the phase in an order that
+// lists every chunk with work first, so chunks with work are spread over the
+// SMs like the slots.  Rewrites the FIFO copy of the record (chunk, sequence,
+// group and their two counters, affine in sequence and group) and returns the
+// index of the instruction it now is.
+DEVI uint32_t balance_attn(const KParams &P, const Smem &S, mk_instr &in, uint32_t idx) {
+  const int B = P.B, G = P.nkv, C = (int)in.nchunk, ch = P.attn_chunk;
+  const int j = ((int)in.chunk * B + in.b) * G + in.g;
+  // sequences whose position reaches chunk c: those with pos >= c * ch
+  auto live = [&](int c) {
+    int n = 0;
+    for (int b = 0; b < B; ++b) n += S.pos[b] >= c * ch;
+    return n;
+  };
+  int nreal = 0;
+  for (int c = 0; c < C; ++c) nreal += live(c) * G;
+  const bool want_real = j < nreal;
+  int r = want_real ? j : j - nreal;  // rank among the chunks with (without) work
+  int c = 0;
+  for (; c < C; ++c) {
+    const int n = (want_real ? live(c) : B - live(c)) * G;
+    if (r < n) break;
+    r -= n;
+  }
+  // the (r / G)-th sequence of chunk c with (without) work, group r % G
+  int b = 0, k = r / G;
+  for (; b < B; ++b)
+    if ((S.pos[b] >= c * ch) == want_real && k-- == 0) break;
+  const int g = r % G;
+  const int jn = (c * B + b) * G + g;
+  in.sig_ctr = in.sig_ctr + (uint32_t)((b - (int)in.b) * G + (g - (int)in.g));
+  in.wait_ctr = in.wait_ctr + (uint32_t)(g - (int)in.g);
+  in.chunk = (uint32_t)c;
+  in.b = (uint16_t)b;
+  in.g = (uint16_t)g;
+  return idx - (uint32_t)j + (uint32_t)jn;
+}
+
+template <bool TC>
 DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   const uint64_t pol = policy_evict_first();
   const uint32_t N = P.n_instr, E = P.ring_pages, PG = P.page_bytes;
@@ -422,10 +466,13 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
           uint4 *dst = reinterpret_cast<uint4 *>(&S.fifo[f]);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = ra[i];
+          uint32_t idx = a;
+          if (TC && P.mode == kModeStatic && S.fifo[f].op == MK_OP_ATTN)  // (batch > 1)
+            idx = balance_attn(P, S, S.fifo[f], a);
           const mk_instr &in = S.fifo[f];
           const uint32_t np = n_pages(P, S, in);
           SlotMeta &m = S.meta[f];
-          m.idx = a;
+          m.idx = idx;
           m.seq0 = seq_c;
           m.npages = np;
           m.t_claim = (P.flags & MK_FLAG_TRACE) ? gtimer() : 0ull;
@@ -1679,7 +1726,7 @@ DEVI void megakernel_body(const KParams &P) {
     tc_fence_after();
   }
   if (warp == 0) {
-    if (lane == 0) loader(P, S, epoch);
+    if (lane == 0) loader<TC>(P, S, epoch);
     __syncwarp();
   } else if (warp == 1) {
     storer(P, S, epoch, lane);

@@ -332,9 +332,16 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     }
     // attention chunks, group-major
     new_phase(MK_OP_ATTN, l);
-    for (int grp = 0; grp < nkv; ++grp)
-      for (int b = 0; b < B; ++b)
-        for (uint32_t ck = 0; ck < P.nchunk; ++ck) {
+    // batch > 1: chunk-major, then sequence, then group, the order the kernel
+    // re-deals at run time (static lists) so that chunks with work (a ragged
+    // batch's early chunks) spread evenly over the SMs.  Batch 1 keeps
+    // group-major order: a group's chunks follow its QKV tiles.
+    const uint32_t n_att = P.nchunk * (uint32_t)B * (uint32_t)nkv;
+    for (uint32_t jj = 0; jj < n_att; ++jj) {
+        const uint32_t ck = B > 1 ? jj / ((uint32_t)B * nkv) : jj % P.nchunk;
+        const int b = B > 1 ? (int)((jj / nkv) % B) : 0;
+        const int grp = B > 1 ? (int)(jj % nkv) : (int)(jj / P.nchunk);
+        {
           mk_instr in = base(MK_OP_ATTN, l);
           in.b = (uint16_t)b;
           in.g = (uint16_t)grp;
@@ -349,6 +356,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
           P.ctr_inc[in.sig_ctr]++;
           if (ck == 0) P.ctr_inc[in.sig2_ctr]++;
         }
+    }
     // O-projection + residual
     new_phase(MK_OP_OPROJ, l);
     P.off_o[l] = off;

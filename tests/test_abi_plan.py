@@ -125,6 +125,31 @@ def test_tensor_core_tiles_split_along_k_in_whole_balanced_slices(name):
         mk.mk_destroy(p)
 
 
+@pytest.mark.parametrize("name", [n for n in ORDER if WORKLOADS[n]["batch"] > 1])
+def test_attention_records_allow_the_run_time_redeal(name):
+    """Batch > 1: the kernel re-deals a layer's attention slots at run time
+    (static lists) by rewriting a record's chunk, sequence and group and shifting its
+    two counters: that needs the phase in (chunk, sequence, group) order and
+    the counters affine in sequence and group within a layer."""
+    w = WORKLOADS[name]
+    B, G = w["batch"], w["model"]["n_kv_heads"]
+    p = host_plan(name)
+    try:
+        rec, _, _ = mk.mk_plan_tables(p)
+        idx = np.nonzero(rec["op"] == mk.MK_OP_ATTN)[0]
+        for l in np.unique(rec["layer"][idx]):
+            ii = idx[rec["layer"][idx] == l]
+            assert np.array_equal(ii, np.arange(ii[0], ii[0] + len(ii)))  # contiguous
+            r = rec[ii]
+            j = (r["chunk"].astype(np.int64) * B + r["b"]) * G + r["g"]
+            assert np.array_equal(j, np.arange(len(ii)))  # (chunk, sequence, group) order
+            assert len(np.unique(r["wait_ctr"].astype(np.int64) - r["g"])) == 1
+            assert len(np.unique(r["sig_ctr"].astype(np.int64) - (r["b"].astype(np.int64) * G + r["g"]))) == 1
+            assert len(np.unique(r["sig2_ctr"])) == 1 and len(np.unique(r["wait_tgt"])) == 1
+    finally:
+        mk.mk_destroy(p)
+
+
 def test_fault_flag_makes_one_target_unreachable():
     w = WORKLOADS["tiny"]
     p = host_plan("tiny", flags=mk.MK_FLAG_FAULT_WAIT)
