@@ -332,15 +332,19 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     }
     // attention chunks, group-major
     new_phase(MK_OP_ATTN, l);
-    // batch > 1: chunk-major, then sequence, then group, the order the kernel
-    // re-deals at run time (static lists) so that chunks with work (a ragged
-    // batch's early chunks) spread evenly over the SMs.  Batch 1 keeps
-    // group-major order: a group's chunks follow its QKV tiles.
+    // Order of the phase.  Where it takes several rounds of the SMs (and in
+    // every batched plan): chunk-major, then sequence, then group, so that
+    // dealt round-robin each group's chunks spread over the rounds alike and
+    // every group's merge comes at about the same time; batched plans also
+    // re-deal this order at run time (static lists) so that chunks with work
+    // (a ragged batch's early chunks) spread evenly.  One round at batch 1:
+    // group-major, a group's chunks next to each other.
     const uint32_t n_att = P.nchunk * (uint32_t)B * (uint32_t)nkv;
+    const bool chunk_major = B > 1 || n_att > num_sms;
     for (uint32_t jj = 0; jj < n_att; ++jj) {
-        const uint32_t ck = B > 1 ? jj / ((uint32_t)B * nkv) : jj % P.nchunk;
-        const int b = B > 1 ? (int)((jj / nkv) % B) : 0;
-        const int grp = B > 1 ? (int)(jj % nkv) : (int)(jj / P.nchunk);
+        const uint32_t ck = chunk_major ? jj / ((uint32_t)B * nkv) : jj % P.nchunk;
+        const int b = chunk_major ? (int)((jj / nkv) % B) : 0;
+        const int grp = chunk_major ? (int)(jj % nkv) : (int)(jj / P.nchunk);
         {
           mk_instr in = base(MK_OP_ATTN, l);
           in.b = (uint16_t)b;
