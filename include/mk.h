@@ -273,9 +273,13 @@ MK_API int mk_read_counters(mk_plan_t plan, uint32_t *counters, uint32_t *queue,
 
 /* With MK_FLAG_TRACE: n_instr records of 10 u64 {sm id << 32 | block,
    t_published, t_ready, t_done, t_pages_issued, t_compute_done,
-   t_storer_start, t_input_loaded, t_first_page, t_last_page}
-   (%globaltimer ns) of the last step; the last three are recorded for
-   batch-1 GEMV instructions only. */
+   t_storer_start, s1, s2, s3} (%globaltimer ns) of the last step.  The
+   stage stamps s1..s3: a batch-1 GEMV, input in registers, first page
+   present, last page present; a tensor-core tile, MMA loop entered, first
+   page present, last page's B operand present; an attention chunk with work,
+   query and current row loaded, scores done, value page present.  Stage
+   stamps older than t_ready were left by an earlier instruction (an empty
+   attention chunk records none). */
 MK_API int mk_read_trace(mk_plan_t plan, uint64_t *trace);
 
 MK_API int mk_debug_buffers(mk_plan_t plan, mk_debug_buffers_t *out);
