@@ -851,19 +851,40 @@ DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const Slo
 // block's last slice: out(r, b) = the sum over slices, in slice order, of the
 // slices' partial sums; then RoPE and the KV append (q/k/v rows), the
 // residual (O, down), SiLU(gate) * up, or the logits.
-__device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
-                                         int tid) {
+__device__ __noinline__ bool tc_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
+                                         int tid, int lane, uint32_t &xbar_uses) {
   const OpGeom &G = P.geom[in.op];
   const int B = P.B, MR = (int)G.MR, NSL = (int)in.nchunk, d = P.d;
   const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
   const float *gp = P.gpart + (size_t)rb * NSL * MR * B;
-  auto val = [&](int r, int b) {
-    float v = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < NSL; ++s) v += __ldcg(gp + ((size_t)s * MR + r) * B + b);
-    return v;
-  };
   constexpr int T = kComputeWarps * 32;
+  // 1. every (row, sequence) sum of the slices, in slice order, into shared
+  //    memory (the attention scratch, idle during a projection): a thread's
+  //    three outputs and four slices of each in flight at once, so the gather
+  //    costs about one round trip to L2
+  float *sums = S.opart;  // [MR][B]
+  const int nsum = MR * B;
+  for (int o0 = tid; o0 < nsum; o0 += 3 * T) {
+    float v[3] = {0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < NSL; s0 += 4) {
+      float w[3][4];
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          w[k][t] = (o0 + k * T < nsum && s0 + t < NSL)
+                        ? __ldcg(gp + (size_t)(s0 + t) * MR * B + o0 + k * T) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 3; ++k)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) v[k] += w[k][t];
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      if (o0 + k * T < nsum) sums[o0 + k * T] = v[k];
+  }
+  if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
+  auto val = [&](int r, int b) { return sums[r * B + b]; };
   switch (in.op) {
     case MK_OP_QKV: {
       const int GR = (P.qpg + 2) * d, half = d / 2, npairs = (int)in.nrows / 2;
@@ -893,15 +914,32 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
       break;
     }
     case MK_OP_OPROJ:
-    case MK_OP_DOWN:
-      for (int u = tid; u < (int)in.nrows * B; u += T) {
-        const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
-        const float resid = (in.op == MK_OP_OPROJ && (in.flags & 1))
-                                ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
-                                : __ldcg(P.x + (size_t)b * P.H + row);
-        P.x[(size_t)b * P.H + row] = resid + val(r, b);
+    case MK_OP_DOWN: {
+      const int n = (int)in.nrows * B;
+      const bool emb = in.op == MK_OP_OPROJ && (in.flags & 1);
+      for (int u0 = tid; u0 < n; u0 += 3 * T) {  // three residual loads in flight
+        float resid[3];
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int u = u0 + k * T;
+          resid[k] = 0.f;
+          if (u < n) {
+            const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
+            resid[k] = emb ? bf1(P.embed[(size_t)S.tok[b] * P.H + row])
+                           : __ldcg(P.x + (size_t)b * P.H + row);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int u = u0 + k * T;
+          if (u < n) {
+            const int r = u % in.nrows, b = u / in.nrows, row = in.row0 + r;
+            P.x[(size_t)b * P.H + row] = resid[k] + val(r, b);
+          }
+        }
       }
       break;
+    }
     case MK_OP_GATEUP:  // rows interleave gate j (2j) and up j (2j + 1)
       for (int u = tid; u < (int)in.nrows * B; u += T) {
         const int j = u % in.nrows, b = u / in.nrows;
@@ -916,6 +954,7 @@ __device__ __noinline__ void tc_epilogue(const KParams &P, const Smem &S, const 
       }
       break;
   }
+  return true;
 }
 
 // One batch > 1 projection tile: MR weight rows x the input columns of
@@ -1090,7 +1129,7 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
   if (unsplit) {  // the tile owns its rows: finish them and signal the phase
     if (!direct) {
-      tc_epilogue(P, S, in, tid);
+      if (!tc_epilogue(P, S, in, tid, lane, xbar_uses)) return false;
       if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
     }
     if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig_ctr * kCtrStride, 1u);
@@ -1103,7 +1142,7 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   }
   if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
   if (S.misc[2]) {
-    tc_epilogue(P, S, in, tid);
+    if (!tc_epilogue(P, S, in, tid, lane, xbar_uses)) return false;
     if (!compute_sync(P, S, S.xbar, xbar_uses, lane)) return false;
     if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
   }

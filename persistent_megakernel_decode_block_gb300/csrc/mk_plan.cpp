@@ -468,6 +468,8 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // attention: per-warp partials {o[d]} and {m, l}, double-buffered, then
   // per-warp scores
   uint32_t att_bytes = (2 * kComputeWarps * d + 2 * kComputeWarps * 2 + kComputeWarps * P.att_lmax) * 4;
+  // tensor-core plans also gather a split block's slice sums here (MR x B)
+  if (P.tc) att_bytes = std::max<uint32_t>(att_bytes, 128u * (uint32_t)B * 4u);
   uint32_t rel_att = take(att_bytes, 16);
   uint32_t rel_sat = take(P.n_wait * 4, 16);
   uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
