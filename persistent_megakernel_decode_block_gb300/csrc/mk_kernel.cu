@@ -746,8 +746,7 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
   for (int b = cw; b < P.B; b += kComputeWarps) {  // a warp per sequence
     float r = 1.f;
     if (norm) {
-      // normalised inputs are x or an embedding row: 16 values of a lane in
-      // flight per round trip
+      // normalised inputs are x or an embedding row
       float ss = 0.f;
       if (emb) {
         const uint16_t *row = P.embed + (size_t)S.tok[b] * P.H;
@@ -765,16 +764,17 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
         }
       } else {
         const float *row = P.x + (size_t)b * P.H;
-        for (uint32_t c = lane * 8; c < G.K; c += 512) {
-          const bool two = c + 256 < G.K;
-          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float4 a0 = __ldcg(reinterpret_cast<const float4 *>(row + c));
-          const float4 a1 = __ldcg(reinterpret_cast<const float4 *>(row + c + 4));
-          const float4 a2 = two ? __ldcg(reinterpret_cast<const float4 *>(row + c + 256)) : z;
-          const float4 a3 = two ? __ldcg(reinterpret_cast<const float4 *>(row + c + 260)) : z;
-          const float4 q[4] = {a0, a1, a2, a3};
+        for (uint32_t c = lane * 8; c < G.K; c += 1024) {  // 32 values of a lane in flight
+          float4 q[8];
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
+            const bool in_k = c + 256 * t < G.K;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            q[2 * t] = in_k ? __ldcg(reinterpret_cast<const float4 *>(row + c + 256 * t)) : z;
+            q[2 * t + 1] = in_k ? __ldcg(reinterpret_cast<const float4 *>(row + c + 256 * t + 4)) : z;
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
             ss = fmaf(q[t].x, q[t].x, ss);
             ss = fmaf(q[t].y, q[t].y, ss);
             ss = fmaf(q[t].z, q[t].z, ss);
@@ -984,27 +984,14 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   const OpGeom &G = P.geom[in.op];
   const int B = P.B, NB = P.tc_nb, MR = (int)G.MR, kc = (int)G.kc;
   const int tid = cw * 32 + lane;
-  const uint32_t key = input_key(in);
-  if (key != xkey) {
-    ++key_changes;
-    if (!norm_factors(P, S, in, cw, lane, xbar_uses, S.normr + (key_changes & 1u) * kMaxBatch))
-      return false;
-    xkey = key;
-  }
-  const float *normr = S.normr + (key_changes & 1u) * kMaxBatch;
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const uint16_t *gain = gain_of(P, in.op, in.layer);
   uint8_t *bop = reinterpret_cast<uint8_t *>(S.xs);
   const uint32_t slot_bytes = (uint32_t)kc * (uint32_t)NB * 2u;
   const int c0 = in.nchunk > 1 ? (int)(in.chunk * G.kp / in.nchunk) * kc : 0;
   const uint32_t where = kWhereCompute | meta.idx, np = meta.npages, b0 = bseq;
-  // 1. B operand of page q (rows >= 2B stay zero from the kernel's start),
-  //    written by compute warps 1.. (warp 0 issues the MMAs).  The producer
-  //    threads form NG groups of one (sequence, 8 columns) unit each; group
-  //    g owns pages g, g + NG, ... and fetches its next page's activations
-  //    right after storing one, so each fetch has NG pages' time to land.
-  //    Every producer warp arrives on every slot (after the wait for the
-  //    slot's previous MMAs), so a slot's count never depends on ownership.
+  // producer geometry (step 1 below); a producer's first page of activations
+  // is fetched before the norm factors, so the two round trips overlap
   const int units = B * (kc / 8), pt = tid - 32;
   const int NG = ((kComputeWarps - 1) * 32) / units;  // >= 1 (checked by the planner)
   const int grp = pt >= 0 ? pt / units : NG;
@@ -1014,6 +1001,22 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   auto fetch = [&](uint32_t q) {
     if (has && q < np) load8(P, S, in.op, emb, ub, c0 + (int)q * kc + uk, v);
   };
+  if (cw != 0) fetch((uint32_t)grp);
+  const uint32_t key = input_key(in);
+  if (key != xkey) {
+    ++key_changes;
+    if (!norm_factors(P, S, in, cw, lane, xbar_uses, S.normr + (key_changes & 1u) * kMaxBatch))
+      return false;
+    xkey = key;
+  }
+  const float *normr = S.normr + (key_changes & 1u) * kMaxBatch;
+  // 1. B operand of page q (rows >= 2B stay zero from the kernel's start),
+  //    written by compute warps 1.. (warp 0 issues the MMAs).  The producer
+  //    threads form NG groups of one (sequence, 8 columns) unit each; group
+  //    g owns pages g, g + NG, ... and fetches its next page's activations
+  //    right after storing one, so each fetch has NG pages' time to land.
+  //    Every producer warp arrives on every slot (after the wait for the
+  //    slot's previous MMAs), so a slot's count never depends on ownership.
   auto store = [&](uint32_t q) -> bool {
     const uint32_t n = b0 + q, bs = n % kTcBufs;
     if (n >= (uint32_t)kTcBufs &&
@@ -1048,8 +1051,7 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   };
   if (cw != 0) {
     // 2a. producers: every page's slot, in order (at most kTcBufs ahead of
-    //     the MMAs through the slots' release)
-    fetch((uint32_t)grp);
+    //     the MMAs through the slots' release; the first fetch went out above)
     for (uint32_t q = 0; q < np; ++q)
       if (!store(q)) return false;
   } else {
