@@ -150,6 +150,28 @@ def test_attention_records_allow_the_run_time_redeal(name):
         mk.mk_destroy(p)
 
 
+@pytest.mark.parametrize("name", ORDER)
+def test_attention_phase_order(name):
+    """A layer's attention chunks are chunk-major (then sequence, then group)
+    wherever the phase takes more than one round of the SMs or the plan is
+    batched, group-major (then chunk) otherwise."""
+    w = WORKLOADS[name]
+    B, G = w["batch"], w["model"]["n_kv_heads"]
+    p = host_plan(name)
+    try:
+        rec, _, _ = mk.mk_plan_tables(p)
+        r = rec[(rec["op"] == mk.MK_OP_ATTN) & (rec["layer"] == 0)]
+        C = int(r["nchunk"][0])
+        chunk_major = B > 1 or len(r) > 152
+        if chunk_major:
+            j = (r["chunk"].astype(np.int64) * B + r["b"]) * G + r["g"]
+        else:
+            j = r["g"].astype(np.int64) * C + r["chunk"]
+        assert np.array_equal(j, np.arange(len(r)))
+    finally:
+        mk.mk_destroy(p)
+
+
 def test_fault_flag_makes_one_target_unreachable():
     w = WORKLOADS["tiny"]
     p = host_plan("tiny", flags=mk.MK_FLAG_FAULT_WAIT)
