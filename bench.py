@@ -43,8 +43,12 @@ def args_():
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--sched", default="static", choices=["dynamic", "static"])
+    p.add_argument("--ring", action="store_true",
+                   help="batch 1: the shared page ring of bulk copies instead of per-warp streams")
     p.add_argument("--no-baselines", action="store_true", help="skip multi-kernel and CPU legs")
     p.add_argument("--trace", default="", help="write a per-instruction trace (npz) here")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: override the workload's layer count (a smaller case)")
     return p.parse_args()
 
 
@@ -63,7 +67,7 @@ def kernel_sha256():
     import glob
     import hashlib
     pat = os.path.join(ROOT, "persistent_megakernel_decode_block_gb300", "csrc", "*")
-    fs = sorted([f for f in glob.glob(pat) if f.endswith((".cu", ".cpp", ".h"))] +
+    fs = sorted([f for f in glob.glob(pat) if f.endswith((".cu", ".cuh", ".cpp", ".h"))] +
                 [os.path.join(ROOT, "include", "mk.h")], key=os.path.basename)
     h = hashlib.sha256()
     for f in fs:
@@ -76,7 +80,7 @@ def kernel_sha256():
 def recorded_traffic(workload):
     """dram bytes read + written per launch from the committed ncu summary of
     this workload, or None when the kernel changed since that capture."""
-    kernel = "mk_megakernel_tc" if WORKLOADS[workload]["batch"] > 1 else "mk_megakernel"
+    kernel = "mk_megakernel_tc" if WORKLOADS[workload]["batch"] > 1 else "mk_megakernel_stream"
     path = os.path.join(ROOT, "profiles", "%s_%s_sections.md" % (kernel, workload))
     try:
         kv = {}
@@ -230,7 +234,9 @@ def run_mine(a):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = WORKLOADS[a.config]
-    m, B, name = w["model"], w["batch"], a.config
+    m, B, name = dict(w["model"]), w["batch"], a.config
+    if a.layers:
+        m["n_layers"] = a.layers
     ctx, mctx = contexts(name, a.seed), max_ctx(name, a.seed)
     span = w["steps"]  # positions ctx .. ctx+span-1 exist in the cache
     weights = make_model(m, a.seed)
@@ -240,7 +246,8 @@ def run_mine(a):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev)
 
     cfg = mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC if a.sched == "static"
-                         else mk.MK_SCHED_DYNAMIC, flags=mk.MK_FLAG_TRACE if a.trace else 0)
+                         else mk.MK_SCHED_DYNAMIC,
+                         flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_RING_B1 if a.ring else 0))
     plan = mk.mk_plan(cfg)
     info = mk.mk_plan_info(plan)
     mk.mk_load_weights(plan, {"embed": up(weights["embed"]), "final_norm": up(weights["final_norm"]),

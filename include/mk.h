@@ -69,6 +69,9 @@ extern "C" {
 #define MK_FLAG_TRACE 0x1u      /* record per-instruction timestamps (mk_read_trace) */
 #define MK_FLAG_HOST_ONLY 0x2u  /* build the tables only; no CUDA call at all */
 #define MK_FLAG_FAULT_WAIT 0x4u /* TEST ONLY: one wait target is made unreachable */
+#define MK_FLAG_RING_B1 0x8u    /* batch 1: stream weights through the block's shared page
+                                   ring (one loader thread's bulk copies, the pages' loader
+                                   role) instead of per-warp rings; kept for comparison */
 
 #define MK_SCHED_DYNAMIC 0 /* global work queue, one atomic claim per instruction */
 #define MK_SCHED_STATIC 1  /* per-SM lists, round-robin over the queue order */
@@ -143,6 +146,10 @@ typedef struct mk_plan_info_s {
   uint32_t attn_chunk;      /* max positions per chunk */
   uint64_t arena_bytes;     /* re-tiled weights held by the plan */
   uint64_t weight_bytes;    /* algorithmic weight bytes streamed per step */
+  uint32_t warp_ring_slots; /* batch-1 stream plans: 512-byte slots in each compute warp's
+                               ring (0: the plan uses the shared page ring) */
+  uint32_t kernel;          /* 0 shared page ring (batch 1), 1 tensor cores (batch > 1),
+                               2 per-warp streams (batch 1, the default) */
 } mk_plan_info_t;
 
 /* Weights in PyTorch layout ([out, in] row-major, bf16 bit patterns), as host

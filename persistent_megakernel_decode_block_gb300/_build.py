@@ -8,7 +8,7 @@ import tempfile
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["mk_kernel.cu", "mk_runtime.cu", "mk_plan.cpp", "mk_noalloc.cu"]
+SOURCES = ["mk_kernel.cu", "mk_stream.cu", "mk_runtime.cu", "mk_plan.cpp", "mk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include"), "-I", os.path.join(HERE, "csrc")]

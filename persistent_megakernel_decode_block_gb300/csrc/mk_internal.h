@@ -22,6 +22,10 @@ constexpr int kMaxChunks = 4;   // 256-column chunks per item: the input slice a
 constexpr int kTcBufs = 4;     // ring slots of the tensor-core B operand (one page's columns each)
 constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
 constexpr int kMaxRing = 32;
+// stream plans: each compute warp's ring of 512-byte slots is filled by
+// per-lane async copies in commit groups of kSG slots
+constexpr int kSG = 4;
+constexpr int kMaxWarpRing = 32;  // slots per warp ring (at most 8 commit groups in flight)
 // block flags (bail, bad input) at the start of the misc area, then the
 // table of the block's shared-memory pointers
 constexpr int kMiscDescOffset = 64, kMiscDescBytes = 256;
@@ -65,6 +69,8 @@ struct KParams {
   int32_t L, H, nq, nkv, d, F, V, B, max_ctx, qpg;
   int32_t nchunk, attn_chunk, att_lmax;
   int32_t tc, tc_nb;  // tensor-core projections (batch > 1); MMA N = 2 x batch rounded up to 16
+  int32_t stream;     // batch 1: compute warps stream their own weights (per-warp rings)
+  uint32_t wnb;       // stream plans: slots (512 B) in each compute warp's ring
   float *gpart;       // partial sums of split projections [block][slice][MR][B]
   float eps, attn_scale;
   int32_t n_wait, mode;
@@ -76,7 +82,7 @@ struct KParams {
   // dynamic shared-memory layout (byte offsets)
   uint32_t ring_pages, page_bytes;
   uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,
-      off_rope, off_normr, off_misc, off_rbuf, off_xs, smem_total;
+      off_rope, off_normr, off_misc, off_rbuf, off_xs, off_wring, smem_total;
 };
 
 // per FIFO slot metadata written by the loader
@@ -98,6 +104,12 @@ cudaError_t launch_retile_tc(uint8_t *dst, const uint8_t *src, const int32_t *ma
 cudaError_t launch_retile(uint8_t *dst, const uint8_t *src, const int32_t *map,
                           const uint64_t *rowtab, uint32_t nrows, const OpGeom &g, uint32_t page,
                           cudaStream_t stream);
+cudaError_t launch_retile_stream(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                                 const uint64_t *rowtab, uint32_t nrows, const OpGeom &g,
+                                 cudaStream_t stream);
+cudaError_t set_stream_smem(uint32_t bytes);
+cudaError_t launch_megakernel_stream(const KParams &P, uint32_t grid, bool cooperative,
+                                     cudaStream_t stream);
 #endif
 
 }  // namespace mk

@@ -123,6 +123,10 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // phase within one tile per SM; the last slice of a block to finish sums
   // the slices (in slice order) and applies the epilogue.
   P.tc = B > 1;
+  // Batch 1: every compute warp streams its own share of each tile through a
+  // private ring of 512-byte slots (per-lane async copies), unless the plan
+  // asks for the shared page ring fed by the loader's bulk copies.
+  P.stream = B == 1 && !(c.flags & MK_FLAG_RING_B1);
   if (P.tc) {
     P.tc_nb = 16 * cdiv(2 * (uint32_t)B, 16);
     const uint32_t rows_of[8] = {0, (uint32_t)(nkv * GR), 0, (uint32_t)H, (uint32_t)(2 * F),
@@ -174,6 +178,11 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
           toff += (uint64_t)P.geom[op].kp * page;
           continue;
         }
+        if (P.stream) {  // items in (slice, row) order: offset << 24 | rows << 12 | row
+          for (uint32_t r = 0; r < w; ++r) rt.push_back((toff << 24) | ((uint64_t)w << 12) | r);
+          toff += (uint64_t)w * P.geom[op].NS * P.geom[op].item_bytes;
+          continue;
+        }
         for (uint32_t r = 0; r < w; ++r) rt.push_back(toff | r);
         toff += (uint64_t)tile_pages(op, w) * page;
       }
@@ -185,17 +194,102 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // instruction streams two pages and indexes rows without division.
   // Automatic size: one page, halved (down to 64 positions) while the
   // attention phase would occupy fewer than half of the SMs.
+  // Stream plans: a warp's keys and values of a chunk must fit its ring
+  // (checked once the ring size is known); start from 128 positions at
+  // d = 64 and 64 at d = 128.
   const uint32_t rpp = page / (2 * (uint32_t)d);  // key (or value) rows per page
-  uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : rpp;
+  const uint32_t ch_cap = P.stream ? (d == 64 ? 128u : 64u) : rpp;
+  uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : ch_cap;
   if (c.attn_chunk <= 0)
     while (ch > 64 && (uint64_t)B * nkv * cdiv(c.max_ctx, ch) < num_sms / 2) ch /= 2;
-  if (ch % 16 || ch < 16 || ch > rpp)
+  if (ch % 16 || ch < 16 || (!P.stream && ch > rpp) || ch > 1024)
     REJECT("attn_chunk must be a multiple of 16 and at most one page of keys");
   P.attn_chunk = ch;
   P.nchunk = cdiv(c.max_ctx, ch);
   // each compute warp keeps the scores of its share of a chunk; a head has
   // at least kComputeWarps / qpg warps
   P.att_lmax = (uint32_t)align_up(cdiv(ch, (uint32_t)(kComputeWarps / qpg)), 4);
+
+  // ---- shared-memory layout -------------------------------------------------
+  // per-slot dot products (items x batch); also the size of the storer's residual buffer
+  P.res_floats = P.tc ? 4u : (uint32_t)align_up((uint64_t)tile_items_max * B, 4);
+  uint32_t fixed = 0;
+  auto take = [&](uint32_t bytes, uint32_t align) {
+    fixed = (uint32_t)align_up(fixed, align);
+    uint32_t at = fixed;
+    fixed += bytes;
+    return at;
+  };
+  // offsets are relative to the end of the ring; rebased below
+  uint32_t rel_fifo = take(kFifo * 64, 64);
+  uint32_t rel_meta = take(kFifo * sizeof(SlotMeta), 16);
+  uint32_t rel_res = take(kFifo * P.res_floats * 4, 16);
+  // attention: per-warp partials {o[d]} and {m, l}, double-buffered, then
+  // per-warp scores
+  uint32_t att_bytes = (2 * kComputeWarps * d + 2 * kComputeWarps * 2 + kComputeWarps * P.att_lmax) * 4;
+  // tensor-core plans also gather a split block's slice sums here (MR x B)
+  if (P.tc) att_bytes = std::max<uint32_t>(att_bytes, 128u * (uint32_t)B * 4u);
+  uint32_t rel_att = take(att_bytes, 16);
+  uint32_t rel_sat = take((uint32_t)L * (nkv + 4) * 4, 16);  // the waited counters
+  uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
+  uint32_t rel_rope = take(B * d * 4, 16);
+  uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
+  uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
+  uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
+  // staged GEMV input (normalised x, or the attention output) and attention scores
+  uint32_t xs_floats = std::max<uint32_t>(H, QD);
+  if (P.tc)  // the MMA's B operand, one page's columns (kc x N bf16) per ring slot
+    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
+      if (op != MK_OP_ATTN)
+        xs_floats = std::max<uint32_t>(xs_floats, kTcBufs * P.geom[op].kc * P.tc_nb / 2);
+  uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
+  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4 + 2 * kTcBufs) * 8;
+  uint32_t rel_bars = take(bars_max, 8);
+  uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
+  uint32_t ring;
+  if (P.stream) {  // per-warp rings of 512-byte slots, whole commit groups
+    P.ring_pages = 0;
+    P.wnb = std::min<uint32_t>(kMaxWarpRing, avail / (kComputeWarps * 512u)) / kSG * kSG;
+    // an item (its slots plus a partly filled group) must fit
+    const uint32_t nch_max = std::max(P.geom[MK_OP_QKV].nch, std::max(P.geom[MK_OP_OPROJ].nch,
+                             std::max(P.geom[MK_OP_DOWN].nch, P.geom[MK_OP_LMHEAD].nch)));
+    if (P.wnb < 2 * nch_max + kSG) REJECT("shared memory too small for the per-warp rings");
+    // a warp's keys and values of one attention chunk must fit its ring
+    const uint32_t nqs_min = (uint32_t)(kComputeWarps - qpg) / (uint32_t)qpg + 1u;
+    auto fits = [&](uint32_t cpos) {
+      const uint32_t rows = cdiv(cpos, nqs_min);
+      const uint32_t chunks = 2u * cdiv((uint64_t)rows * d * 2u, 512u);
+      return cdiv(chunks, kSG) * kSG <= P.wnb;
+    };
+    if (!fits(P.attn_chunk)) {
+      if (c.attn_chunk > 0) REJECT("attn_chunk too large for the per-warp rings");
+      while (P.attn_chunk > 16 && !fits(P.attn_chunk)) P.attn_chunk /= 2;
+      if (!fits(P.attn_chunk)) REJECT("per-warp rings too small for an attention chunk");
+      P.nchunk = cdiv(c.max_ctx, P.attn_chunk);
+      P.att_lmax = (uint32_t)align_up(cdiv(P.attn_chunk, (uint32_t)(kComputeWarps / qpg)), 4);
+    }
+    ring = (uint32_t)align_up((uint64_t)kComputeWarps * P.wnb * 512u, 1024);
+  } else {
+    uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);
+    if (E < 2) REJECT("shared memory too small for a two-page ring");
+    P.ring_pages = E;
+    ring = (uint32_t)align_up(E * page, 1024);
+  }
+  P.off_wring = 0;
+  P.off_fifo = ring + rel_fifo;
+  P.off_meta = ring + rel_meta;
+  P.off_res = ring + rel_res;
+  P.off_att = ring + rel_att;
+  P.off_sat = ring + rel_sat;
+  P.off_pos = ring + rel_pos;
+  P.off_rope = ring + rel_rope;
+  P.off_normr = ring + rel_normr;
+  P.off_misc = ring + rel_misc;
+  P.off_rbuf = ring + rel_rbuf;
+  P.off_xs = ring + rel_xs;
+  P.off_bars = ring + rel_bars;
+  P.smem_total = ring + fixed;
+  if (P.smem_total > smem_limit) REJECT("shared-memory layout exceeds the limit");
 
   // ---- counters ----------------------------------------------------------
   P.n_wait = (uint32_t)L * (nkv + 4);
@@ -222,7 +316,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     bool plain = page % g.item_bytes == 0;
     const std::vector<uint32_t> &t = P.tiles[MK_OP_LMHEAD];
     for (size_t i = 0; i + 1 < t.size(); ++i) plain = plain && (t[i] * g.NS) % g.ipp == 0;
-    P.embed_alias = c.tie_embeddings && plain && !P.tc;
+    P.embed_alias = c.tie_embeddings && plain && !P.tc && !P.stream;
   }
   if (!P.embed_alias) {
     P.off_embed = off;
@@ -264,6 +358,14 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     const OpGeom &g = P.geom[op];
     const uint32_t wrows = wrows_of(op, in.nrows);
     P.weight_bytes += (uint64_t)wrows * g.K * 2;
+    if (P.stream) {  // items of the tile back to back, (slice, row) order
+      in.npages = 0;
+      in.wofs = off;
+      off += (uint64_t)wrows * g.NS * g.item_bytes;
+      push(in);
+      P.ctr_inc[in.sig_ctr]++;
+      return;
+    }
     if (!P.tc) {
       in.npages = tile_pages(op, wrows);
       in.wofs = off;
@@ -451,60 +553,6 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     }
   }
 
-  // ---- shared-memory layout -------------------------------------------------
-  // per-slot dot products (items x batch); also the size of the storer's residual buffer
-  P.res_floats = P.tc ? 4u : (uint32_t)align_up((uint64_t)tile_items_max * B, 4);
-  uint32_t fixed = 0;
-  auto take = [&](uint32_t bytes, uint32_t align) {
-    fixed = (uint32_t)align_up(fixed, align);
-    uint32_t at = fixed;
-    fixed += bytes;
-    return at;
-  };
-  // offsets are relative to the end of the ring; rebased below
-  uint32_t rel_fifo = take(kFifo * 64, 64);
-  uint32_t rel_meta = take(kFifo * sizeof(SlotMeta), 16);
-  uint32_t rel_res = take(kFifo * P.res_floats * 4, 16);
-  // attention: per-warp partials {o[d]} and {m, l}, double-buffered, then
-  // per-warp scores
-  uint32_t att_bytes = (2 * kComputeWarps * d + 2 * kComputeWarps * 2 + kComputeWarps * P.att_lmax) * 4;
-  // tensor-core plans also gather a split block's slice sums here (MR x B)
-  if (P.tc) att_bytes = std::max<uint32_t>(att_bytes, 128u * (uint32_t)B * 4u);
-  uint32_t rel_att = take(att_bytes, 16);
-  uint32_t rel_sat = take(P.n_wait * 4, 16);
-  uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
-  uint32_t rel_rope = take(B * d * 4, 16);
-  uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
-  uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
-  uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
-  // staged GEMV input (normalised x, or the attention output) and attention scores
-  uint32_t xs_floats = std::max<uint32_t>(H, QD);
-  if (P.tc)  // the MMA's B operand, one page's columns (kc x N bf16) per ring slot
-    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
-      if (op != MK_OP_ATTN)
-        xs_floats = std::max<uint32_t>(xs_floats, kTcBufs * P.geom[op].kc * P.tc_nb / 2);
-  uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
-  uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4 + 2 * kTcBufs) * 8;
-  uint32_t rel_bars = take(bars_max, 8);
-  uint32_t avail = smem_limit > fixed + 1024 ? smem_limit - fixed - 1024 : 0;
-  uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);
-  if (E < 2) REJECT("shared memory too small for a two-page ring");
-  P.ring_pages = E;
-  uint32_t ring = (uint32_t)align_up(E * page, 1024);
-  P.off_fifo = ring + rel_fifo;
-  P.off_meta = ring + rel_meta;
-  P.off_res = ring + rel_res;
-  P.off_att = ring + rel_att;
-  P.off_sat = ring + rel_sat;
-  P.off_pos = ring + rel_pos;
-  P.off_rope = ring + rel_rope;
-  P.off_normr = ring + rel_normr;
-  P.off_misc = ring + rel_misc;
-  P.off_rbuf = ring + rel_rbuf;
-  P.off_xs = ring + rel_xs;
-  P.off_bars = ring + rel_bars;
-  P.smem_total = ring + fixed;
-  if (P.smem_total > smem_limit) REJECT("shared-memory layout exceeds the limit");
 #undef REJECT
   return MK_OK;
 }

@@ -29,13 +29,15 @@ struct HostPlan {
   uint32_t n_wait = 0, n_ctr = 0, lm_ctr = 0;
   uint32_t attn_chunk = 0, nchunk = 0, att_lmax = 0;
   bool tc = false;              // batch > 1: projections on tcgen05, split along K
+  bool stream = false;          // batch 1: every compute warp streams its own weights
+  uint32_t wnb = 0;             // stream plans: ring slots (512 B) per compute warp
   uint32_t tc_nb = 0;           // MMA N: 2 x batch (value and remainder) rounded up to 16
   uint64_t gpart_floats = 0;    // partial-sum buffer of split projections
   uint32_t gemv_arr_base = 0;   // arrival counters of split row blocks
   // shared-memory layout
   uint32_t ring_pages = 0, page_bytes = 0, res_floats = 0;
   uint32_t off_bars = 0, off_fifo = 0, off_meta = 0, off_res = 0, off_att = 0, off_sat = 0,
-           off_pos = 0, off_rope = 0, off_normr = 0, off_misc = 0, off_rbuf = 0, off_xs = 0, smem_total = 0;
+           off_pos = 0, off_rope = 0, off_normr = 0, off_misc = 0, off_rbuf = 0, off_xs = 0, off_wring = 0, smem_total = 0;
   uint32_t fault_instr = 0xFFFFFFFFu;
 };
 

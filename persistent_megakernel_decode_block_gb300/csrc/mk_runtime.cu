@@ -155,7 +155,7 @@ static int setup_device(mk_plan_s *p) {
     CK(cudaMemcpy(p->d_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CK(cudaMemcpy(p->d_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
   }
-  CK(set_megakernel_smem(H.smem_total));
+  CK(H.stream ? set_stream_smem(H.smem_total) : set_megakernel_smem(H.smem_total));
 
   KParams &P = p->base;
   memset(&P, 0, sizeof P);
@@ -194,6 +194,9 @@ static int setup_device(mk_plan_s *p) {
   P.att_lmax = (int32_t)H.att_lmax;
   P.tc = H.tc ? 1 : 0;
   P.tc_nb = (int32_t)H.tc_nb;
+  P.stream = H.stream ? 1 : 0;
+  P.wnb = H.wnb;
+  P.off_wring = H.off_wring;
   P.gpart = p->d_gpart;
   P.eps = c.rms_eps;
   P.attn_scale = (float)(1.0 / sqrt((double)d));
@@ -303,6 +306,8 @@ MK_API int mk_plan_info(mk_plan_t p, mk_plan_info_t *info) {
   info->attn_chunk = H.attn_chunk;
   info->arena_bytes = H.arena_bytes;
   info->weight_bytes = H.weight_bytes;
+  info->warp_ring_slots = H.stream ? H.wnb : 0u;
+  info->kernel = H.stream ? 2u : H.tc ? 1u : 0u;
   return MK_OK;
 }
 
@@ -387,6 +392,9 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
     cudaError_t e;
     if (H.tc) {
       e = launch_retile_tc(dst, stage, map, rows, H.geom[op], pg, s);
+    } else if (H.stream) {
+      if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
+      e = launch_retile_stream(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], s);
     } else {
       if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
       e = launch_retile(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], pg, s);
@@ -457,7 +465,9 @@ MK_API int mk_decode_step(mk_plan_t p, const int32_t *tokens, const int32_t *pos
   if (rc != MK_OK) return rc;
   cudaSetDevice(p->device);
   const KParams P = step_params(p, tokens, positions, kv, logits);
-  if (launch_megakernel(P, p->H.num_sms, true, (cudaStream_t)stream) != cudaSuccess) {
+  const cudaError_t le = P.stream ? launch_megakernel_stream(P, p->H.num_sms, true, (cudaStream_t)stream)
+                                  : launch_megakernel(P, p->H.num_sms, true, (cudaStream_t)stream);
+  if (le != cudaSuccess) {
     (void)cudaGetLastError();
     return MK_ERR_LAUNCH;
   }
@@ -489,7 +499,9 @@ static int enqueue_phases(mk_plan_t p, const KParams &base, cudaStream_t s, int 
     const mk_phase &ph = p->H.phases[i];
     P.range_first = ph.first;
     P.range_count = ph.count;
-    if (launch_megakernel(P, ph.count, false, s) != cudaSuccess) {
+    const cudaError_t le = P.stream ? launch_megakernel_stream(P, ph.count, false, s)
+                                    : launch_megakernel(P, ph.count, false, s);
+    if (le != cudaSuccess) {
       (void)cudaGetLastError();
       return MK_ERR_LAUNCH;
     }

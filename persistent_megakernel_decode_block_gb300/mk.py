@@ -21,7 +21,7 @@ for _c, _n in ERRORS.items():
     globals()[_n] = _c
 MK_OP_QKV, MK_OP_ATTN, MK_OP_OPROJ, MK_OP_GATEUP, MK_OP_DOWN, MK_OP_LMHEAD = 1, 2, 3, 4, 5, 6
 MK_NO_COUNTER = 0xFFFFFFFF
-MK_FLAG_TRACE, MK_FLAG_HOST_ONLY, MK_FLAG_FAULT_WAIT = 1, 2, 4
+MK_FLAG_TRACE, MK_FLAG_HOST_ONLY, MK_FLAG_FAULT_WAIT, MK_FLAG_RING_B1 = 1, 2, 4, 8
 MK_SCHED_DYNAMIC, MK_SCHED_STATIC = 0, 1
 
 _i32, _u32, _f32, _vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_void_p
@@ -40,7 +40,8 @@ class mk_plan_info_t(ctypes.Structure):
     _fields_ = [(n, _u32) for n in ("n_instr", "n_counters", "n_wait_counters", "n_phases",
                                     "n_blocks", "threads", "ring_pages", "page_bytes",
                                     "fifo_depth", "smem_bytes", "attn_nchunk", "attn_chunk")] + [
-        ("arena_bytes", ctypes.c_uint64), ("weight_bytes", ctypes.c_uint64)]
+        ("arena_bytes", ctypes.c_uint64), ("weight_bytes", ctypes.c_uint64),
+        ("warp_ring_slots", _u32), ("kernel", _u32)]
 
 
 class mk_phase(ctypes.Structure):
