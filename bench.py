@@ -43,8 +43,8 @@ def args_():
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--sched", default="static", choices=["dynamic", "static"])
-    p.add_argument("--ring", action="store_true",
-                   help="batch 1: the shared page ring of bulk copies instead of per-warp streams")
+    p.add_argument("--stream", action="store_true",
+                   help="batch 1: per-warp streams of async copies instead of the shared page ring")
     p.add_argument("--no-baselines", action="store_true", help="skip multi-kernel and CPU legs")
     p.add_argument("--trace", default="", help="write a per-instruction trace (npz) here")
     p.add_argument("--layers", type=int, default=0,
@@ -80,7 +80,7 @@ def kernel_sha256():
 def recorded_traffic(workload):
     """dram bytes read + written per launch from the committed ncu summary of
     this workload, or None when the kernel changed since that capture."""
-    kernel = "mk_megakernel_tc" if WORKLOADS[workload]["batch"] > 1 else "mk_megakernel_stream"
+    kernel = "mk_megakernel_tc" if WORKLOADS[workload]["batch"] > 1 else "mk_megakernel"
     path = os.path.join(ROOT, "profiles", "%s_%s_sections.md" % (kernel, workload))
     try:
         kv = {}
@@ -247,7 +247,7 @@ def run_mine(a):
 
     cfg = mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC if a.sched == "static"
                          else mk.MK_SCHED_DYNAMIC,
-                         flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_RING_B1 if a.ring else 0))
+                         flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_STREAM_B1 if a.stream else 0))
     plan = mk.mk_plan(cfg)
     info = mk.mk_plan_info(plan)
     mk.mk_load_weights(plan, {"embed": up(weights["embed"]), "final_norm": up(weights["final_norm"]),

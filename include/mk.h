@@ -69,9 +69,10 @@ extern "C" {
 #define MK_FLAG_TRACE 0x1u      /* record per-instruction timestamps (mk_read_trace) */
 #define MK_FLAG_HOST_ONLY 0x2u  /* build the tables only; no CUDA call at all */
 #define MK_FLAG_FAULT_WAIT 0x4u /* TEST ONLY: one wait target is made unreachable */
-#define MK_FLAG_RING_B1 0x8u    /* batch 1: stream weights through the block's shared page
-                                   ring (one loader thread's bulk copies, the pages' loader
-                                   role) instead of per-warp rings; kept for comparison */
+#define MK_FLAG_STREAM_B1 0x8u  /* batch 1: every compute warp streams its own weights through
+                                   a private ring of per-lane async copies, instead of the
+                                   block's shared page ring fed by the loader warp's bulk
+                                   copies (the default); an alternative kept for comparison */
 
 #define MK_SCHED_DYNAMIC 0 /* global work queue, one atomic claim per instruction */
 #define MK_SCHED_STATIC 1  /* per-SM lists, round-robin over the queue order */
@@ -146,10 +147,10 @@ typedef struct mk_plan_info_s {
   uint32_t attn_chunk;      /* max positions per chunk */
   uint64_t arena_bytes;     /* re-tiled weights held by the plan */
   uint64_t weight_bytes;    /* algorithmic weight bytes streamed per step */
-  uint32_t warp_ring_slots; /* batch-1 stream plans: 512-byte slots in each compute warp's
-                               ring (0: the plan uses the shared page ring) */
-  uint32_t kernel;          /* 0 shared page ring (batch 1), 1 tensor cores (batch > 1),
-                               2 per-warp streams (batch 1, the default) */
+  uint32_t warp_ring_slots; /* MK_FLAG_STREAM_B1 plans: 512-byte slots in each compute
+                               warp's ring (0: the plan uses the shared page ring) */
+  uint32_t kernel;          /* 0 shared page ring (batch 1, the default), 1 tensor cores
+                               (batch > 1), 2 per-warp streams (batch 1, MK_FLAG_STREAM_B1) */
 } mk_plan_info_t;
 
 /* Weights in PyTorch layout ([out, in] row-major, bf16 bit patterns), as host
@@ -320,7 +321,10 @@ MK_API void mk_destroy(mk_plan_t plan);
    capture.  All calls share the array: calls that overlap on the GPU race.
    Asynchronous on `stream`; calls no allocating routine.  Errors: MK_ERR_ARG
    (NULL pointer, unsupported shape, too large for the scratch),
-   MK_ERR_DEVICE, MK_ERR_CUDA, MK_ERR_LAUNCH. */
+   MK_ERR_DEVICE, MK_ERR_CUDA (also: a CUDA error was already pending when
+   the call began; it is left pending for the caller and nothing is
+   launched), MK_ERR_LAUNCH (a launch was rejected; a rejected first launch
+   queues nothing after it). */
 MK_API int mk_attention_noalloc(const float *q, const void *k_cache, const void *v_cache,
                                 const int32_t *positions, float *out, int32_t batch,
                                 int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,

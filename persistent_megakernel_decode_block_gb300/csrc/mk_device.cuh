@@ -30,14 +30,17 @@ DEVI void mbar_arrive_expect_tx(uint64_t *b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes)
                : "memory");
 }
+// Potentially blocking: the thread may be suspended (up to the hint, 20 us)
+// until the phase completes, so a waiting warp does not take issue slots
+// from the warps sharing its scheduler; false if the phase is still open.
 DEVI bool mbar_try_wait(uint64_t *b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(saddr(b)), "r"(parity)
+      : "r"(saddr(b)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }

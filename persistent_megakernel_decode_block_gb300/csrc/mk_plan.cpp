@@ -123,10 +123,10 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // phase within one tile per SM; the last slice of a block to finish sums
   // the slices (in slice order) and applies the epilogue.
   P.tc = B > 1;
-  // Batch 1: every compute warp streams its own share of each tile through a
-  // private ring of 512-byte slots (per-lane async copies), unless the plan
-  // asks for the shared page ring fed by the loader's bulk copies.
-  P.stream = B == 1 && !(c.flags & MK_FLAG_RING_B1);
+  // Batch 1 on request: every compute warp streams its own share of each tile
+  // through a private ring of 512-byte slots (per-lane async copies) instead
+  // of the shared page ring fed by the loader's bulk copies.
+  P.stream = B == 1 && (c.flags & MK_FLAG_STREAM_B1);
   if (P.tc) {
     P.tc_nb = 16 * cdiv(2 * (uint32_t)B, 16);
     const uint32_t rows_of[8] = {0, (uint32_t)(nkv * GR), 0, (uint32_t)H, (uint32_t)(2 * F),

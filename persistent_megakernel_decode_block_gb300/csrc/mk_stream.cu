@@ -39,6 +39,16 @@ DEVI void cp_async16(void *dst, const void *src) {
 DEVI void cp_async16_s(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// one commit group's four slots: 16 bytes each at dst + 512 t from src + 512 t
+DEVI void cp_async16x4(uint32_t dst, const void *src) {
+  asm volatile(
+      "cp.async.cg.shared.global [%0], [%1], 16;\n\t"
+      "cp.async.cg.shared.global [%0+512], [%1+512], 16;\n\t"
+      "cp.async.cg.shared.global [%0+1024], [%1+1024], 16;\n\t"
+      "cp.async.cg.shared.global [%0+1536], [%1+1536], 16;" ::"r"(dst),
+      "l"(src)
+      : "memory");
+}
 DEVI void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // 16-byte load from a shared-window address (an explicit shared-space load,
 // never a generic one)
@@ -188,6 +198,19 @@ DEVI void issue_more(const KParams &P, const Smem &S, WStream &W, int cw, int la
       W.gl = R.ctot / kSG;
       W.state = 1u;
     }
+    if (W.r0 >= (int32_t)(kSG * 512)) {  // a whole group of range 0 (the common case)
+      cp_async16x4(W.ring + W.islot * 512u, W.p0);
+      W.p0 += kSG * 512;
+      W.r0 -= kSG * 512;
+      W.islot = W.islot + kSG == W.nb ? 0u : W.islot + kSG;
+      cp_commit();
+      W.iss += kSG;
+      if (--W.gl == 0u) {
+        ++W.fi;
+        W.state = 0u;
+      }
+      continue;
+    }
     const int32_t me = lane * 16;
 #pragma unroll
     for (int t = 0; t < kSG; ++t) {
@@ -227,54 +250,70 @@ DEVI bool wait_upto(const KParams &P, const Smem &S, WStream &W, uint32_t c, int
 }
 
 // ------------------------------------------------------------------ GEMV ----
-// X: the warp's input values for one slice (lane l, chunk j: columns
-// s SW + 256 j + 8 l .. + 7), from the staged input or, for the down
-// projection, straight from h.
-DEVI void load_x_slice(const KParams &P, const Smem &S, int op, uint32_t s, int lane, float r,
-                       XCache &X) {
+// The dot product runs on packed pairs of fp32 (fma.rn.f32x2): the two bf16
+// of a weight word, widened exactly, times two consecutive inputs.
+struct XPack {
+  unsigned long long p[kSG][4];  // chunk j, pair m: inputs (8 m' + 2 m, + 1) of the lane's slice
+};
+DEVI unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+DEVI float sum2(unsigned long long v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a + b;
+}
+// acc += (lo bf16 of w, hi bf16 of w) * (x0, x1), elementwise in fp32
+DEVI void fma_bf2(unsigned long long &acc, uint32_t w, unsigned long long xp) {
+  asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 wp;\n\t"
+      "shl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xFFFF0000;\n\t"
+      "mov.b64 wp, {lo, hi};\n\tfma.rn.f32x2 %0, wp, %2, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(w), "l"(xp));
+}
+DEVI void load_x_pack(const KParams &P, const Smem &S, int op, uint32_t s, int lane, float r,
+                      XPack &X) {
   const OpGeom &G = P.geom[op];
 #pragma unroll
-  for (int j = 0; j < kMaxChunks; ++j)
-    if (j < (int)G.nch) {
-      const uint32_t col = s * G.SW + (uint32_t)j * 256u + (uint32_t)lane * 8u;
-      float4 a, c;
-      if (op == MK_OP_DOWN) {
-        a = __ldcg(reinterpret_cast<const float4 *>(P.h + col));
-        c = __ldcg(reinterpret_cast<const float4 *>(P.h + col + 4));
-      } else {
-        const uint32_t xa = saddr(S.xs + col);
-        const uint4 ua = lds128(xa), uc = lds128(xa + 16);
-        a = make_float4(__uint_as_float(ua.x), __uint_as_float(ua.y), __uint_as_float(ua.z),
-                        __uint_as_float(ua.w));
-        c = make_float4(__uint_as_float(uc.x), __uint_as_float(uc.y), __uint_as_float(uc.z),
-                        __uint_as_float(uc.w));
-        a.x *= r; a.y *= r; a.z *= r; a.w *= r;
-        c.x *= r; c.y *= r; c.z *= r; c.w *= r;
-      }
-      X.v[j][0] = a.x; X.v[j][1] = a.y; X.v[j][2] = a.z; X.v[j][3] = a.w;
-      X.v[j][4] = c.x; X.v[j][5] = c.y; X.v[j][6] = c.z; X.v[j][7] = c.w;
+  for (int j = 0; j < kSG; ++j) {
+    if ((uint32_t)j >= G.nch) break;
+    const uint32_t col = s * G.SW + (uint32_t)j * 256u + (uint32_t)lane * 8u;
+    float4 a, c;
+    if (op == MK_OP_DOWN) {
+      a = __ldcg(reinterpret_cast<const float4 *>(P.h + col));
+      c = __ldcg(reinterpret_cast<const float4 *>(P.h + col + 4));
+    } else {
+      const uint32_t xa = saddr(S.xs + col);
+      const uint4 ua = lds128(xa), uc = lds128(xa + 16);
+      a = make_float4(__uint_as_float(ua.x) * r, __uint_as_float(ua.y) * r,
+                      __uint_as_float(ua.z) * r, __uint_as_float(ua.w) * r);
+      c = make_float4(__uint_as_float(uc.x) * r, __uint_as_float(uc.y) * r,
+                      __uint_as_float(uc.z) * r, __uint_as_float(uc.w) * r);
     }
+    X.p[j][0] = pack2(a.x, a.y);
+    X.p[j][1] = pack2(a.z, a.w);
+    X.p[j][2] = pack2(c.x, c.y);
+    X.p[j][3] = pack2(c.z, c.w);
+  }
 }
-
-// one item: nch slots from ring slot `slot` on (advanced past them), this
-// lane's 16 bytes each
-DEVI float dot_ring(const WStream &W, uint32_t &slot, const XCache &X, int nch) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+// one item: nch (<= kSG) consecutive slots from ring byte `soff` on (advanced
+// past them), this lane's 16 bytes of each
+DEVI float dot_item(uint32_t ring, uint32_t &soff, uint32_t rbytes, uint32_t nch,
+                    const XPack &X) {
+  unsigned long long A = 0ull, B = 0ull;  // packed (+0, +0)
 #pragma unroll
-  for (int j = 0; j < kMaxChunks; ++j)
-    if (j < nch) {
-      const uint4 w = lds128(W.ring + slot * 512u);
-      a0 = fmaf(bf_lo(w.x), X.v[j][0], a0);
-      a1 = fmaf(bf_hi(w.x), X.v[j][1], a1);
-      a2 = fmaf(bf_lo(w.y), X.v[j][2], a2);
-      a3 = fmaf(bf_hi(w.y), X.v[j][3], a3);
-      a0 = fmaf(bf_lo(w.z), X.v[j][4], a0);
-      a1 = fmaf(bf_hi(w.z), X.v[j][5], a1);
-      a2 = fmaf(bf_lo(w.w), X.v[j][6], a2);
-      a3 = fmaf(bf_hi(w.w), X.v[j][7], a3);
-      slot = slot + 1 == W.nb ? 0u : slot + 1;
+  for (int j = 0; j < kSG; ++j)
+    if ((uint32_t)j < nch) {
+      const uint4 w = lds128(ring + soff);
+      fma_bf2(A, w.x, X.p[j][0]);
+      fma_bf2(B, w.y, X.p[j][1]);
+      fma_bf2(A, w.z, X.p[j][2]);
+      fma_bf2(B, w.w, X.p[j][3]);
+      soff = soff + 512u == rbytes ? 0u : soff + 512u;
     }
-  return (a0 + a1) + (a2 + a3);
+  return sum2(A) + sum2(B);
 }
 
 // Stage the input of a normalised projection (x, or the embedding row of the
@@ -323,8 +362,7 @@ DEVI bool gemv_stream(const KParams &P, const Smem &S, const mk_instr &in, const
   uint32_t a, b, wrows;
   gemv_share(P, in, cw, a, b, wrows);
   const uint32_t epos = W.con, nch = G.nch;
-  XCache X;  // the input slice, loaded at the first item and at every change of slice
-  uint32_t xs_ = 0xFFFFFFFFu;
+  uint32_t xs_ = 0xFFFFFFFFu;  // slice whose inputs are in Xp
   // 1/rms of a normalised input, from the staging warps' sums of squares
   float r = 1.f;
   if (gain_of(P, in.op, in.layer) != nullptr) {
@@ -334,10 +372,15 @@ DEVI bool gemv_stream(const KParams &P, const Smem &S, const mk_instr &in, const
   }
   const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
   SlotMeta &mw = const_cast<SlotMeta &>(meta);  // meta is this entry's slot in shared memory
-  uint32_t s = a / wrows, rr = a - s * wrows, slot = W.cslot;  // item a: row rr, slice s
+  // Items two at a time where they share a slice; the two sums reduced
+  // together (lanes 0..15 end with the first, 16..31 with the second).
+  XPack Xp;
+  uint32_t s = a / wrows, rr = a - s * wrows;
+  uint32_t soff = W.cslot * 512u;  // ring byte of the next item's first slot (this lane's part)
+  const uint32_t rbytes = W.nb * 512u;
   for (uint32_t i = a; i < b;) {
     if (s != xs_) {
-      load_x_slice(P, S, in.op, s, lane, r, X);
+      load_x_pack(P, S, in.op, s, lane, r, Xp);
       xs_ = s;
     }
     if (stamp && i == a) mw.t_input = gtimer();
@@ -345,19 +388,15 @@ DEVI bool gemv_stream(const KParams &P, const Smem &S, const mk_instr &in, const
     const uint32_t cl = W.con + (two ? 2u : 1u) * nch - 1u;
     if (!wait_upto(P, S, W, cl, cw, lane)) return false;
     if (stamp && i == a) mw.t_page0 = gtimer();
-    float acc = dot_ring(W, slot, X, (int)nch);
-    float acc2 = two ? dot_ring(W, slot, X, (int)nch) : 0.f;
+    const float acc = dot_item(W.ring, soff, rbytes, nch, Xp);
+    const float acc2 = two ? dot_item(W.ring, soff, rbytes, nch, Xp) : 0.f;
+    const bool up = (lane & 16) != 0;
+    float v = (up ? acc2 : acc) + __shfl_xor_sync(0xFFFFFFFFu, up ? acc : acc2, 16);
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-      acc2 += __shfl_xor_sync(0xFFFFFFFFu, acc2, o);
-    }
-    if (lane == 0) {
-      res[rr * G.NS + s] = acc;
-      if (two) res[(rr + 1) * G.NS + s] = acc2;
-    }
+    for (int o = 8; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0) res[rr * G.NS + s] = v;
+    if (two && lane == 16) res[(rr + 1) * G.NS + s] = v;
     W.con = cl + 1u;
-    W.cslot = slot;
     const uint32_t n = two ? 2u : 1u;
     i += n;
     rr += n;
@@ -369,7 +408,7 @@ DEVI bool gemv_stream(const KParams &P, const Smem &S, const mk_instr &in, const
   if (stamp) mw.t_pagel = gtimer();
   // skip the instruction's padding slots; refill the ring
   const uint32_t ctot = ((b - a) * nch + kSG - 1) / kSG * kSG;
-  W.cslot = slot_add(W.cslot, epos + ctot - W.con, W.nb);
+  W.cslot = slot_add(soff / 512u, epos + ctot - W.con, W.nb);
   W.con = epos + ctot;
   issue_more(P, S, W, cw, lane);
   return true;
@@ -421,9 +460,9 @@ __device__ __noinline__ bool attn_stream(const KParams &P, const Smem &S, const 
   // current position's key slice and value dims if this warp covers p_b
   float q8[8], kn8[8], vn[DPL];
   {
-    const float *qh = P.q + ((size_t)b * P.nq + (size_t)g * QPG + h) * D + part * 8;
-    const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(qh));
-    const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(qh + 4));
+    const size_t qo = ((size_t)b * P.nq + (size_t)g * QPG + h) * D + part * 8;
+    const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(P.q + qo));
+    const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(P.q + qo + 4));
     const float sc = P.attn_scale;
     q8[0] = x0.x * sc; q8[1] = x0.y * sc; q8[2] = x0.z * sc; q8[3] = x0.w * sc;
     q8[4] = x1.x * sc; q8[5] = x1.y * sc; q8[6] = x1.z * sc; q8[7] = x1.w * sc;
