@@ -57,6 +57,8 @@ def lib():
                               ctypes.c_char_p, i]),
             "or_simulate": (i, [vp, i, i, i, i, ctypes.c_uint64, i, vp, vp, ctypes.c_char_p, i]),
             "or_explore": (ctypes.c_long, [vp, i, i, i, ctypes.c_long, ctypes.c_char_p, i]),
+            "or_redeal": (i, [vp, i, ctypes.POINTER(_Shape), i, vp, vp, i, vp, ctypes.c_char_p,
+                              i]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -201,3 +203,25 @@ def explore(table, n_instr, n_counters, fifo_depth, max_states=2_000_000):
     if n < 0:
         raise AssertionError("explore: " + msg.value.decode())
     return n
+
+
+def redeal(table, n_instr, cfg, batch, attn_chunk, positions, list_idx=None):
+    """Executed instruction of every list slot (uint32 array, the order of
+    list_idx, or of the queue when list_idx is None) once each batched
+    attention phase is re-dealt for `positions`: chunks with work first.
+    Raises AssertionError when the table does not allow the re-deal."""
+    table = np.ascontiguousarray(table, dtype=np.uint8)
+    assert table.size == 64 * n_instr
+    s = _Shape(cfg["n_layers"], cfg["hidden"], cfg["n_q_heads"], cfg["n_kv_heads"],
+               cfg["head_dim"], cfg["ffn_dim"], cfg["vocab"], batch)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    assert pos.size == batch
+    li = None if list_idx is None else np.ascontiguousarray(list_idx, dtype=np.uint32)
+    out = np.zeros(n_instr, dtype=np.uint32)
+    msg = ctypes.create_string_buffer(512)
+    rc = lib().or_redeal(table.ctypes.data, n_instr, ctypes.byref(s), int(attn_chunk),
+                         pos.ctypes.data, None if li is None else li.ctypes.data, n_instr,
+                         out.ctypes.data, msg, 512)
+    if rc != 0:
+        raise AssertionError("redeal: " + msg.value.decode())
+    return out

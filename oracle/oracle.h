@@ -37,4 +37,7 @@ int or_simulate(const void *table, int n_instr, int n_counters, int S, int fifo_
                 char *msg, int msg_len);
 long or_explore(const void *table, int n_instr, int n_counters, int fifo_depth, long max_states,
                 char *msg, int msg_len);
+int or_redeal(const void *table, int n_instr, const or_shape *s, int attn_chunk,
+              const int32_t *positions, const uint32_t *list_idx, int n_list,
+              uint32_t *exec_idx, char *msg, int msg_len);
 #endif

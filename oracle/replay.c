@@ -676,3 +676,105 @@ done:
   free(pend);
   return rc < 0 ? rc : nstates;
 }
+
+/* ---- run-time re-deal of batched attention slots ---------------------------
+ * In batched plans run from static per-SM lists, whether an attention chunk
+ * has keys to read depends on its sequence's position, known only when the
+ * step runs.  So the slots of each layer's attention phase are re-dealt at
+ * run time: the phase's instructions are listed with every chunk that has
+ * work first and every empty chunk after, each part in queue order, and the
+ * list slot holding the phase's j-th instruction executes the j-th of that
+ * listing instead.  A chunk c of sequence b covers positions
+ * [c * chunk, min((c + 1) * chunk, pos_b + 1)); it has work when that range
+ * is not empty.
+ *
+ * Checked here, from the table alone:
+ *  - each attention phase (a run of attention records of one layer) lists
+ *    chunk-major, then sequence, then group, every (chunk, sequence, group)
+ *    once;
+ *  - the records of a phase differ only in chunk, sequence, group, their
+ *    signal counter (one arrival counter per (sequence, group), consecutive
+ *    in group, then sequence) and their wait counter (one per group,
+ *    consecutive), so rewriting those fields of one record by the slot's
+ *    offsets gives exactly the record of the instruction it is re-dealt to;
+ *  - the executed lists are a partition of the queue in which every entry
+ *    stays in its own phase.
+ * Writes the executed index of every list slot to exec_idx (n_list entries;
+ * list_idx may be NULL for the queue order itself, n_list = n_instr). */
+int or_redeal(const void *table, int N, const or_shape *s, int attn_chunk,
+              const int32_t *positions, const uint32_t *list_idx, int n_list,
+              uint32_t *exec_idx, char *msg, int msg_len) {
+  const int B = s->B, G = s->nkv;
+  if (N <= 0 || B <= 0 || G <= 0 || attn_chunk <= 0 || n_list != N)
+    return fail(msg, msg_len, "bad arguments");
+  rec_t *r = (rec_t *)malloc(sizeof(rec_t) * (size_t)N);
+  int *target = (int *)malloc(sizeof(int) * (size_t)N);  /* queue index -> executed index */
+  int *order = (int *)malloc(sizeof(int) * (size_t)N);
+  unsigned char *seen = (unsigned char *)calloc((size_t)N, 1);
+  int rc = 0;
+  for (int i = 0; i < N; ++i) {
+    decode(table, i, &r[i]);
+    target[i] = i;
+  }
+  for (int a = 0; a < N && rc == 0;) {
+    if (r[a].op != OATTN) {
+      ++a;
+      continue;
+    }
+    int e = a;
+    while (e < N && r[e].op == OATTN && r[e].layer == r[a].layer) ++e;
+    const int n = e - a, C = (int)r[a].nchunk;
+    if (C <= 0 || n != C * B * G) {
+      rc = fail(msg, msg_len, "attention phase at %d: %d records for %d chunks x %d x %d", a, n,
+                C, B, G);
+      break;
+    }
+    for (int j = 0; j < n && rc == 0; ++j) {
+      const rec_t *x = &r[a + j], *f = &r[a];
+      const int c = j / (B * G), b = (j / G) % B, g = j % G;
+      if ((int)x->chunk != c || x->b != b || x->g != g)
+        rc = fail(msg, msg_len, "attention record %d is not chunk-major", a + j);
+      else if (x->flags != f->flags || x->wait_tgt != f->wait_tgt || x->sig2_ctr != f->sig2_ctr ||
+               x->sig2_after != f->sig2_after || x->row0 != f->row0 || x->nrows != f->nrows ||
+               x->nchunk != f->nchunk)
+        rc = fail(msg, msg_len, "attention record %d differs from its phase in a fixed field",
+                  a + j);
+      else if (x->sig_ctr != f->sig_ctr + (uint32_t)(b * G + g))
+        rc = fail(msg, msg_len, "attention record %d: arrival counter not per (sequence, group)",
+                  a + j);
+      else if (x->wait_ctr != f->wait_ctr + (uint32_t)g)
+        rc = fail(msg, msg_len, "attention record %d: wait counter not per group", a + j);
+    }
+    if (rc) break;
+    /* the listing: chunks with work, then empty chunks, each in queue order */
+    int k = 0;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int j = 0; j < n; ++j) {
+        const int c = j / (B * G), b = (j / G) % B;
+        const long first = (long)c * attn_chunk;
+        const long end_ = (long)positions[b] + 1 < first + attn_chunk ? (long)positions[b] + 1
+                                                                       : first + attn_chunk;
+        const int has_work = end_ > first;
+        if (has_work == (pass == 0)) order[k++] = a + j;
+      }
+    for (int j = 0; j < n; ++j) target[a + j] = order[j];
+    a = e;
+  }
+  for (int k = 0; k < n_list && rc == 0; ++k) {
+    const uint32_t q = list_idx ? list_idx[k] : (uint32_t)k;
+    if (q >= (uint32_t)N) {
+      rc = fail(msg, msg_len, "list entry %u out of range", q);
+      break;
+    }
+    const int x = target[q];
+    if (seen[x]++) rc = fail(msg, msg_len, "instruction %d executed twice", x);
+    else if (r[x].op != r[q].op || r[x].layer != r[q].layer)
+      rc = fail(msg, msg_len, "slot of instruction %u moved out of its phase", q);
+    exec_idx[k] = (uint32_t)x;
+  }
+  free(r);
+  free(target);
+  free(order);
+  free(seen);
+  return rc;
+}

@@ -150,6 +150,32 @@ def test_attention_records_allow_the_run_time_redeal(name):
         mk.mk_destroy(p)
 
 
+@pytest.mark.parametrize("name", [n for n in ORDER if WORKLOADS[n]["batch"] > 1])
+def test_redealt_schedule_is_a_partition_and_never_deadlocks(name):
+    """The schedule the batched kernel executes from static lists, once the
+    oracle re-deals each attention phase for the step's positions, is still a
+    partition of the queue and completes under the oracle's simulation, for
+    ragged positions that include 0 and max_ctx - 1."""
+    w = WORKLOADS[name]
+    B, mctx = w["batch"], max_ctx(name)
+    p = host_plan(name, n_sms=40, sched_mode=mk.MK_SCHED_STATIC)
+    try:
+        info = mk.mk_plan_info(p)
+        _, raw, _ = mk.mk_plan_tables(p)
+        off, idx = mk.mk_plan_lists(p)
+        rng = np.random.default_rng(5)
+        for trial in range(4):
+            pos = rng.integers(0, mctx, B).astype(np.int32)
+            pos[0], pos[-1] = 0, mctx - 1
+            ex = oracle.redeal(raw, info["n_instr"], w["model"], B, info["attn_chunk"], pos, idx)
+            assert np.array_equal(np.sort(ex), np.arange(info["n_instr"]))
+            oracle.simulate(raw, info["n_instr"], info["n_counters"], info["n_blocks"],
+                            info["fifo_depth"], seed=trial, trials=2, list_off=off,
+                            list_idx=ex)
+    finally:
+        mk.mk_destroy(p)
+
+
 @pytest.mark.parametrize("name", ORDER)
 def test_attention_phase_order(name):
     """A layer's attention chunks are chunk-major (then sequence, then group)

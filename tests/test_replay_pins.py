@@ -146,3 +146,78 @@ def test_static_lists():
     short[-1] -= 1
     with pytest.raises(AssertionError, match="cover"):
         run(t, n, (short, idx), S=S)
+
+
+# ---- run-time re-deal of batched attention slots ----------------------------
+# A batched table by hand: batch 2, 2 KV groups, 2 chunks of 16 positions.
+# Queue: 0 QKV | 1..8 attention, chunk-major (chunk, sequence, group) | 9 O.
+RB, RG, RCH = 2, 2, 16
+RCFG = dict(CFG, n_layers=1)
+
+
+def redeal_table(mut=None):
+    out = [dict(op=QKV, layer=0, wait=(NONE, 0), sig=0, row0=0, nrows=128)]
+    for c in range(2):
+        for b in range(RB):
+            for g in range(RG):
+                f = dict(op=ATTN, layer=0, b=b, g=g, wait=(10 + g, 2), sig=100 + b * RG + g,
+                         sig2=50, sig2_after=2, chunk=c, nchunk=2)
+                if mut:
+                    mut(c, b, g, f)
+                out.append(f)
+    out.append(dict(op=OPROJ, layer=0, wait=(50, RB * RG), sig=60, row0=0, nrows=128))
+    t = b"".join(rec(**f) for f in out)
+    return np.frombuffer(t, dtype=np.uint8).copy(), len(out)
+
+
+@pytest.mark.parametrize("pos, want", [
+    # every chunk of sequence 0 has work, sequence 1 only its first: as queued
+    ((20, 5), [0, 1, 2, 3, 4, 5, 6, 7, 8, 9]),
+    # sequence 0 ends in chunk 0, sequence 1 reaches chunk 1: its chunk-1
+    # slots move ahead of sequence 0's empty ones
+    ((5, 20), [0, 1, 2, 3, 4, 7, 8, 5, 6, 9]),
+    # the boundary: position 15 is the last of chunk 0, 16 the first of chunk 1
+    ((15, 16), [0, 1, 2, 3, 4, 7, 8, 5, 6, 9]),
+    ((16, 15), [0, 1, 2, 3, 4, 5, 6, 7, 8, 9]),
+    # position 0: only the new key, in chunk 0
+    ((0, 0), [0, 1, 2, 3, 4, 5, 6, 7, 8, 9]),
+    ((0, 31), [0, 1, 2, 3, 4, 7, 8, 5, 6, 9]),
+])
+def test_redeal_lists_chunks_with_work_first(pos, want):
+    t, n = redeal_table()
+    assert oracle.redeal(t, n, RCFG, RB, RCH, pos).tolist() == want
+
+
+def test_redeal_maps_list_slots_and_keeps_each_list_in_its_phases():
+    t, n = redeal_table()
+    idx = np.array([0, 2, 4, 6, 8, 1, 3, 5, 7, 9], np.uint32)  # two lists of five
+    got = oracle.redeal(t, n, RCFG, RB, RCH, (5, 20), idx)
+    assert got.tolist() == [0, 2, 4, 8, 6, 1, 3, 7, 5, 9]
+
+
+@pytest.mark.parametrize("what", ["sig_swap", "wait_shared", "sig2", "group_major", "missing"])
+def test_redeal_rejects_tables_that_do_not_allow_it(what):
+    def mut(c, b, g, f):
+        if what == "sig_swap" and c == 1 and b == 0:   # arrival counters of two groups swapped
+            f["sig"] = 100 + b * RG + (1 - g)
+        if what == "wait_shared" and g == 1:           # every group waits on group 0's counter
+            f["wait"] = (10, 2)
+        if what == "sig2" and c == 1 and b == 1 and g == 1:
+            f["sig2"] = 51
+        if what == "group_major":                      # (group, sequence, chunk) order
+            f["chunk"], f["g"] = g, c
+    if what == "missing":
+        t, n = redeal_table()
+        t = np.concatenate([t[:64 * 8], t[64 * 9:]])  # drop the last attention record
+        n -= 1
+    else:
+        t, n = redeal_table(mut)
+    with pytest.raises(AssertionError):
+        oracle.redeal(t, n, RCFG, RB, RCH, (5, 20))
+
+
+def test_redeal_rejects_a_list_that_repeats_a_slot():
+    t, n = redeal_table()
+    idx = np.array([0, 1, 2, 3, 4, 5, 6, 7, 7, 9], np.uint32)
+    with pytest.raises(AssertionError):
+        oracle.redeal(t, n, RCFG, RB, RCH, (5, 20), idx)
