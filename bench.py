@@ -43,9 +43,13 @@ def args_():
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--sched", default="static", choices=["dynamic", "static"])
+    p.add_argument("--l2kb", type=int, default=0,
+                   help="mk_config.l2_prefetch_kb: KB per block prefetched into L2 ahead of the ring")
     p.add_argument("--stream", action="store_true",
                    help="batch 1: per-warp streams of async copies instead of the shared page ring")
     p.add_argument("--no-baselines", action="store_true", help="skip multi-kernel and CPU legs")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads' lines (ctx 8192, ragged batch 8, Llama-8B)")
     p.add_argument("--trace", default="", help="write a per-instruction trace (npz) here")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: override the workload's layer count (a smaller case)")
@@ -180,6 +184,94 @@ def barrier(td, device=None):
             td.barrier()
 
 
+def cpu_facts():
+    """Threads the host offers and its CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def time_workload(mk, torch, dev, name, a):
+    """Another workload, timed as the headline one (same steps and warm-up,
+    static lists, device-resident inputs, CUDA events on the launching
+    stream, clocks sampled): ms/step, passes/s and roofline fraction."""
+    w = WORKLOADS[name]
+    m, B = w["model"], w["batch"]
+    ctx, mctx = contexts(name, a.seed), max_ctx(name, a.seed)
+    span = w["steps"]
+    weights = make_model(m, a.seed)
+    k0, v0 = make_kv(m, B, mctx, ctx, a.seed)
+
+    def up(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev)
+
+    plan = mk.mk_plan(mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC))
+    try:
+        info = mk.mk_plan_info(plan)
+        mk.mk_load_weights(plan, {"embed": up(weights["embed"]),
+                                  "final_norm": up(weights["final_norm"]),
+                                  "lm_head": None if m["tie_embeddings"] else up(weights["lm_head"]),
+                                  "layers": [{k: up(v) for k, v in lw.items()}
+                                             for lw in weights["layers"]]})
+        del weights
+        torch.cuda.empty_cache()
+        kc, vc = up(k0), up(v0)
+        total = a.warmup + a.steps
+        toks = torch.from_numpy(step_tokens(m, B, total, a.seed)).to(dev)
+        pos_host = np.stack([ctx + (s % span) for s in range(total)]).astype(np.int32)
+        poss = torch.from_numpy(pos_host).to(dev)
+        logits = torch.zeros(B, m["vocab"], dtype=torch.float32, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        for s in range(a.warmup):
+            mk.mk_decode_step(plan, toks[s], poss[s], (kc, vc), logits, stream)
+        stream.synchronize()
+        assert mk.mk_status(plan, stream) == 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        clocks = Clocks(dev.index)
+        with clocks:
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for s in range(a.steps):
+                    mk.mk_decode_step(plan, toks[a.warmup + s], poss[a.warmup + s], (kc, vc),
+                                      logits, stream)
+                e1.record(stream)
+            stream.synchronize()
+        code = mk.mk_status(plan, stream)
+        assert code == 0, mk.mk_error_string(code)
+        ms = e0.elapsed_time(e1) / a.steps
+        bytes_step = float(np.mean([algorithmic_bytes(m, info["weight_bytes"], p)
+                                    for p in pos_host[a.warmup:]]))
+        peak, peak_kind = peaks()
+        achieved = bytes_step / (ms * 1e-3) / 1e9
+        return {"ms_per_step": ms, "passes_per_s": 1000.0 / ms, "batch": B,
+                "tokens_per_s": 1000.0 * B / ms,
+                "roofline": {"achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "bytes_per_step": bytes_step,
+                             "peak_kind": peak_kind + " hbm_gbs"},
+                "kernel": "mk_megakernel_tc" if B > 1 else "mk_megakernel",
+                "clocks": clocks.summary()}
+    finally:
+        mk.mk_destroy(plan)
+        torch.cuda.empty_cache()
+
+
 def cpu_oracle(name, seed, weights, budget_s, max_steps=None):
     """The oracle as it stands on the host cores: one untimed step, then
     steps until ~budget_s of work.  Returns (passes/s, steps timed)."""
@@ -216,9 +308,9 @@ def run_reference(a):
             "n_gpus": a.gpus, "steps": n, "warmup": 1, "ms_per_step": 1000 * dt / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": a.config, "batch": w["batch"]},
-            "cpu_baseline": {"value": rate, "unit": "passes/s", "cores": 1, "kind": "oracle",
-                             "sample": "%d full oracle decode steps of %s (of %d requested)"
-                                       % (n, a.config, a.steps)},
+            "cpu_baseline": dict({"value": rate, "unit": "passes/s", "cores": 1, "kind": "oracle",
+                                  "sample": "%d full oracle decode steps of %s (of %d requested)"
+                                            % (n, a.config, a.steps)}, **cpu_facts()),
             "e2e": {"value": rate, "unit": "passes/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -247,7 +339,8 @@ def run_mine(a):
 
     cfg = mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC if a.sched == "static"
                          else mk.MK_SCHED_DYNAMIC,
-                         flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_STREAM_B1 if a.stream else 0))
+                         flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_STREAM_B1 if a.stream else 0),
+                         l2_prefetch_kb=a.l2kb)
     plan = mk.mk_plan(cfg)
     info = mk.mk_plan_info(plan)
     mk.mk_load_weights(plan, {"embed": up(weights["embed"]), "final_norm": up(weights["final_norm"]),
@@ -345,7 +438,13 @@ def run_mine(a):
         rate, n, dt = cpu_oracle(name, a.seed, weights, 12.0)
         cpu = {"value": rate, "unit": "passes/s", "cores": 1, "kind": "oracle",
                "sample": "%d full oracle decode steps of %s (%.1f s, single thread)" % (n, name, dt)}
+        cpu.update(cpu_facts())
     mk.mk_destroy(plan)
+    del weights, kc, vc
+    torch.cuda.empty_cache()
+    if rank == 0 and not a.no_workloads and name == DEFAULT and not a.layers and not a.trace:
+        extra["workloads"] = {o: time_workload(mk, torch, dev, o, a) for o in
+                              ("llama1b_ctx8192", "llama1b_b8_ragged", "llama8b_ctx2048")}
     if rank != 0:
         return
     line = {

@@ -224,13 +224,20 @@ MK_API int mk_plan_lists(mk_plan_t plan, const uint32_t **list_off, const uint32
 /* Copy and re-tile the weights (host or device pointers, see mk_weights)
    into plan-owned memory: q/k rows are paired for RoPE, gate/up rows are
    interleaved per tile, every tile is laid out as whole shared-memory pages.
+   The pages' statement of the problem (« Résumé exécutif », "Le problème")
+   is batch-1 decode bound by streaming every bf16 weight byte once per
+   step; this call lays the weights out in the order the loader streams them
+   (« 2 · Définition et généalogie », §2.6, "4. L'allocateur de mémoire
+   partagée": pages of a shared-memory ring).
    Synchronises `stream` before returning.  Errors: MK_ERR_ARG, MK_ERR_STATE
    (host-only plan), MK_ERR_NOMEM, MK_ERR_CUDA. */
 MK_API int mk_load_weights(mk_plan_t plan, const mk_weights *w, void *stream);
 
 /* One decode step, asynchronous on `stream`; enqueues exactly one kernel
    launch (grid = n_blocks, one resident block per SM, cooperative launch so
-   the driver refuses a grid that cannot be co-resident).
+   the driver refuses a grid that cannot be co-resident): the whole forward
+   pass in one persistent launch (« 2 · Définition et généalogie », §2.1 and
+   §2.4, persistent threads; §2.6 "1. La persistance").
      tokens    device int32 [B]     token of each sequence
      positions device int32 [B]     position p_b; the step writes K/V at p_b and
                                     attends to positions 0..p_b
@@ -270,12 +277,19 @@ MK_API int mk_run_phase(mk_plan_t plan, int phase, const int32_t *tokens,
 /* Synchronise `stream` and return the first device error latched since the
    last call (MK_ERR_TIMEOUT, MK_ERR_BOUNDS) or MK_OK.  After a device error
    the counters, queue, epoch and execution counts are reset so the plan can
-   run again. */
+   run again.  The pages note that counter waits make progress only while
+   every block is resident (« 2 · Définition et généalogie », §2.6 "1. La
+   persistance" and the chapter's questions on deadlock); every wait here is
+   bounded and reports MK_ERR_TIMEOUT instead of hanging. */
 MK_API int mk_status(mk_plan_t plan, void *stream);
 
 /* Synchronise the device and copy out, for bit-exact checks: counters
    (n_counters u32), the work-queue counter, per-instruction execution counts
-   (n_instr u32) and the step epoch.  Any pointer may be NULL. */
+   (n_instr u32) and the step epoch.  Any pointer may be NULL.  The counters
+   are the dependency counters of « 2 · Définition et généalogie », §2.6 "3.
+   Les compteurs de dépendance" (a producer adds 1 after its data is visible,
+   a consumer waits for a target); the queue is the global work queue of §2.6
+   "5. L'ordonnancement". */
 MK_API int mk_read_counters(mk_plan_t plan, uint32_t *counters, uint32_t *queue, uint32_t *exec,
                             uint32_t *epoch);
 

@@ -12,7 +12,8 @@
  * batch-1 decode of Llama-1B.  The pages give no formula for any of these
  * operations.  Every function below therefore restates the standard Llama
  * decoder definition (RMSNorm, rotate-half RoPE, grouped-query attention,
- * SwiGLU MLP, tied or separate LM head); each reading is listed in the design doc.
+ * SwiGLU MLP, tied or separate LM head), each a reading of the pages where
+ * they leave the formula open.
  *
  * Precision: every intermediate is an IEEE double.  Weights and the KV cache
  * are bf16 (their storage type); a key or value written to the cache is

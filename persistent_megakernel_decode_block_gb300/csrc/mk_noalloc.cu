@@ -158,6 +158,11 @@ extern "C" MK_API int mk_attention_noalloc(const float *q, const void *k_cache,
   const int qpg = n_q_heads / n_kv_heads;
   const size_t need = (size_t)batch * n_kv_heads * nch * (2 * qpg + qpg * head_dim);
   if (need > kScratchFloats) return MK_ERR_ARG;  // larger than the fixed scratch
+  // An error left pending by the caller's own earlier work is reported as
+  // MK_ERR_CUDA and left in place for the caller (peek, not get); each
+  // launch below is checked on its own, so a rejected partial launch returns
+  // before the merge is queued.
+  if (cudaPeekAtLastError() != cudaSuccess) return MK_ERR_CUDA;
   float *scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc != MK_OK) return rc;
@@ -167,6 +172,7 @@ extern "C" MK_API int mk_attention_noalloc(const float *q, const void *k_cache,
       q, static_cast<const uint16_t *>(k_cache), static_cast<const uint16_t *>(v_cache),
       positions, scratch, n_q_heads, n_kv_heads, head_dim, max_ctx, nch, ch,
       (float)(1.0 / sqrt((double)head_dim)));
+  if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;
   noalloc_attn_merge<<<dim3(n_kv_heads, batch), 128, 0, s>>>(
       scratch, positions, out, n_q_heads, n_kv_heads, head_dim, max_ctx, nch);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;

@@ -2,14 +2,18 @@
 callers that cannot allocate device memory themselves, e.g. an engine whose
 GPU memory is all owned by its own allocator.  Its chunk partials live in the
 library's fixed static device array.  Checked through the C ABI against the
-plan-based path that computes the same attention (the attention phase of a
-layer, run alone with mk_run_phase), on two calls in a row, so a second call
-that reuses the shared array must still be right.  Kept in the file pytest
-collects last."""
+oracle's attention (fp64, one query head at a time, on the seeded inputs) and
+against the plan-based path that computes the same attention (the attention
+phase of a layer, run alone with mk_run_phase), on two calls in a row, so a
+second call that reuses the shared array must still be right; head_dim 128
+and an out-of-range position (NaN rows) without a plan.  Kept in the file
+pytest collects last."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
+import synth
 from persistent_megakernel_decode_block_gb300 import mk
 
 from harness import ATOL, RTOL_L2, Setup, compare
@@ -52,6 +56,16 @@ def test_no_alloc_attention_matches_the_plan_path(name):
             mk.mk_run_phase(s.plan, ph, s.tokens, s.positions, (s.kc, s.vc), s.logits)
             assert mk.mk_status(s.plan) == 0
             ref = attn_plan.double().cpu().numpy().reshape(B, -1)
+            # the oracle on the seeded inputs: q as drawn, the layer's cache as generated
+            qh = q.cpu().double().numpy().reshape(B, nq, d)
+            qpg = nq // nkv
+            for b in range(B):
+                n = int(s.ctx[b]) + 1
+                want = np.concatenate([oracle.attention(qh[b, h], s.k0[layer, b, h // qpg, :n],
+                                                        s.v0[layer, b, h // qpg, :n])
+                                       for h in range(nq)])
+                a, l2 = compare(ref[b], want)
+                assert a <= ATOL and l2 <= RTOL_L2, ("plan path vs oracle", layer, b, a, l2)
             kl = s.kc.view(-1)[layer * layer_elems:]
             vl = s.vc.view(-1)[layer * layer_elems:]
             for call in range(2):  # the second call reuses the shared scratch
@@ -62,6 +76,13 @@ def test_no_alloc_attention_matches_the_plan_path(name):
                 for b in range(B):
                     a, l2 = compare(got[b], ref[b])
                     assert a <= ATOL and l2 <= RTOL_L2, (layer, call, b, a, l2)
+                    qh_b = q.cpu().double().numpy().reshape(B, nq, d)[b]
+                    n = int(s.ctx[b]) + 1
+                    want = np.concatenate([oracle.attention(qh_b[h], s.k0[layer, b, h // qpg, :n],
+                                                            s.v0[layer, b, h // qpg, :n])
+                                           for h in range(nq)])
+                    a, l2 = compare(got[b], want)
+                    assert a <= ATOL and l2 <= RTOL_L2, ("no-alloc vs oracle", layer, call, b, a, l2)
     finally:
         s.close()
 
@@ -77,3 +98,32 @@ def test_no_alloc_attention_rejects_what_does_not_fit():
     with pytest.raises(mk.MkError) as e:
         mk.mk_attention_noalloc(x, x, x, p, x, 1, 6, 4, 64, 128)
     assert e.value.code == mk.MK_ERR_ARG
+
+
+def test_no_alloc_attention_head_dim_128_and_out_of_range_rows():
+    """head_dim 128 (the Llama-8B head), 2 KV groups of 4 query heads, a
+    512-position cache; sequences at positions 0, 300 and 511 = max_ctx - 1
+    match the oracle, a sequence at position max_ctx gets NaN rows."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    B, nq, nkv, d, mctx = 4, 8, 2, 128, 512
+    qpg = nq // nkv
+    pos = np.array([0, 300, 511, 512], np.int32)
+    k = synth.normal_bf16(3, 901, (B, nkv, mctx, d))
+    v = synth.normal_bf16(3, 902, (B, nkv, mctx, d))
+    q = torch.randn(B * nq * d, generator=torch.Generator().manual_seed(11))
+    kd = torch.from_numpy(k.view(np.int16)).cuda()
+    vd = torch.from_numpy(v.view(np.int16)).cuda()
+    pd = torch.from_numpy(pos).cuda()
+    out = torch.zeros((B, nq * d), device="cuda")
+    mk.mk_attention_noalloc(q.cuda(), kd, vd, pd, out, B, nq, nkv, d, mctx)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    qh = q.double().numpy().reshape(B, nq, d)
+    for b in range(3):
+        n = int(pos[b]) + 1
+        want = np.concatenate([oracle.attention(qh[b, h], k[b, h // qpg, :n], v[b, h // qpg, :n])
+                               for h in range(nq)])
+        a, l2 = compare(got[b], want)
+        assert a <= ATOL and l2 <= RTOL_L2, (b, a, l2)
+    assert np.isnan(got[3]).all()
