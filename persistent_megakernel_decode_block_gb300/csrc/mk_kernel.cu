@@ -1051,13 +1051,17 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
   if (S.misc[2]) {
     const int PS = 2 * QPG + QPG * D;
     const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
+    // up to MB chunks' partials in flight at once (one round trip to L2 for
+    // a group of up to MB chunks); per batch, the batch's maximum first, then
+    // one rescale of the running sums
+    constexpr int MB = 16;
     for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
       const int h = o / D;
       float M = -INFINITY, den = 0.f, num = 0.f;
-      for (int c0 = 0; c0 < nch; c0 += 8) {
-        float mc[8], lc[8], oc[8];
+      for (int c0 = 0; c0 < nch; c0 += MB) {
+        float mc[MB], lc[MB], oc[MB];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < MB; ++u) {
           mc[u] = -INFINITY;
           lc[u] = oc[u] = 0.f;
           if (c0 + u < nch) {
@@ -1067,15 +1071,21 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
             oc[u] = __ldcg(pc + 2 * QPG + o);
           }
         }
+        float Mb = M;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < MB; ++u) Mb = fmaxf(Mb, mc[u]);
+        if (Mb == -INFINITY) continue;
+        const float a = __expf(M - Mb);
+        den *= a;
+        num *= a;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
           if (mc[u] == -INFINITY) continue;
-          const float Mn = fmaxf(M, mc[u]);
-          const float a = __expf(M - Mn), w = __expf(mc[u] - Mn);
-          den = den * a + w * lc[u];
-          num = num * a + w * oc[u];
-          M = Mn;
+          const float w = __expf(mc[u] - Mb);
+          den = fmaf(w, lc[u], den);
+          num = fmaf(w, oc[u], num);
         }
+        M = Mb;
       }
       P.attn[(size_t)b * P.nq * D + (size_t)g * QPG * D + o] = num / den;
     }
