@@ -264,6 +264,7 @@ def time_workload(mk, torch, dev, name, a):
                 "tokens_per_s": 1000.0 * B / ms,
                 "roofline": {"achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "bytes_per_step": bytes_step,
+                             "traffic": recorded_traffic(name),
                              "peak_kind": peak_kind + " hbm_gbs"},
                 "kernel": "mk_megakernel_tc" if B > 1 else "mk_megakernel",
                 "clocks": clocks.summary()}
@@ -404,7 +405,8 @@ def run_mine(a):
     if a.trace:
         tr = mk.mk_read_trace(plan)
         rec, _, _ = mk.mk_plan_tables(plan)
-        np.savez_compressed(a.trace, trace=tr, op=rec["op"], layer=rec["layer"])
+        np.savez_compressed(a.trace, trace=tr, op=rec["op"], layer=rec["layer"], b=rec["b"],
+                            g=rec["g"], chunk=rec["chunk"], positions=pos_host[-1])
 
     # end to end through the host-buffer entry point: tokens/positions in,
     # logits out, every step, pinned host memory
