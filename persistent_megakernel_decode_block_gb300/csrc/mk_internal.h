@@ -70,6 +70,7 @@ struct KParams {
   int32_t nchunk, attn_chunk, att_lmax;
   int32_t tc, tc_nb;  // tensor-core projections (batch > 1); MMA N = 2 x batch rounded up to 16
   int32_t stream;     // batch 1: compute warps stream their own weights (per-warp rings)
+  int32_t att_grp;    // attention warps serve all query heads of the group (attn_chunk_grp)
   uint32_t wnb;       // stream plans: slots (512 B) in each compute warp's ring
   float *gpart;       // partial sums of split projections [block][slice][MR][B]
   float eps, attn_scale;

@@ -800,6 +800,80 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
   return true;
 }
 
+// Step 6 of an attention chunk, shared by both chunk layouts: the chunk's
+// partial {m, l, o} is in global memory (written before the block barrier
+// this starts with); take the arrival and, for the group's last chunk, merge.
+template <int D, int QPG>
+__device__ __forceinline__ bool attn_arrive_merge(const KParams &P, const Smem &S,
+                                                  const mk_instr &in, int cw, int lane,
+                                                  uint32_t &att_uses, uint32_t epoch, int b,
+                                                  int g, int pos) {
+  // arrival: the chunk that completes its (sequence, group) merges all of
+  //    the group's chunk partials by log-sum-exp, in chunk order, with every
+  //    compute thread (one output each), and
+  //    releases the group counter.  The acq_rel arrival publishes this chunk's
+  //    partial (ordered before it by the barrier) and, for the last arriver,
+  //    acquires every other chunk's.
+  //    Only the nch chunks that reach p_b arrive: the last of them also adds
+  //    the nchunk - nch empty chunks' share, so the counter still advances by
+  //    nchunk per step.
+  const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (cw == 0 && lane == 0) {
+    uint32_t *ctr = P.ctr + (size_t)in.sig_ctr * kCtrStride;
+    const uint32_t old = atom_add_acq_rel(ctr, 1u);
+    const bool last = old == epoch * in.nchunk + (uint32_t)nch - 1u;
+    if (last && (uint32_t)nch < in.nchunk) red_add(ctr, in.nchunk - (uint32_t)nch);
+    S.misc[2] = last ? 1 : 0;
+  }
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (S.misc[2]) {
+    const int PS = 2 * QPG + QPG * D;
+    const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
+    // up to MB chunks' partials in flight at once (one round trip to L2 for
+    // a group of up to MB chunks); per batch, the batch's maximum first, then
+    // one rescale of the running sums
+    constexpr int MB = 16;
+    for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
+      const int h = o / D;
+      float M = -INFINITY, den = 0.f, num = 0.f;
+      for (int c0 = 0; c0 < nch; c0 += MB) {
+        float mc[MB], lc[MB], oc[MB];
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+          mc[u] = -INFINITY;
+          lc[u] = oc[u] = 0.f;
+          if (c0 + u < nch) {
+            const float *pc = pb + (size_t)(c0 + u) * PS;
+            mc[u] = __ldcg(pc + h);
+            lc[u] = __ldcg(pc + QPG + h);
+            oc[u] = __ldcg(pc + 2 * QPG + o);
+          }
+        }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) Mb = fmaxf(Mb, mc[u]);
+        if (Mb == -INFINITY) continue;
+        const float a = __expf(M - Mb);
+        den *= a;
+        num *= a;
+#pragma unroll
+        for (int u = 0; u < MB; ++u) {
+          if (mc[u] == -INFINITY) continue;
+          const float w = __expf(mc[u] - Mb);
+          den = fmaf(w, lc[u], den);
+          num = fmaf(w, oc[u], num);
+        }
+        M = Mb;
+      }
+      P.attn[(size_t)b * P.nq * D + (size_t)g * QPG * D + o] = num / den;
+    }
+    if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+    if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
+  }
+  return true;
+}
+
 // One split-KV attention chunk for the QPG query heads of group g of
 // sequence b over its positions [p0, p1): scores q.k/sqrt(d), the chunk's
 // maximum m, denominator l = sum exp(s - m) and unnormalised output
@@ -1029,75 +1103,258 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
     }
   }
 
-  // 6. arrival: the chunk that completes its (sequence, group) merges all of
-  //    the group's chunk partials by log-sum-exp, in chunk order, with every
-  //    compute thread (one output each, eight chunks' loads in flight), and
-  //    releases the group counter.  The acq_rel arrival publishes this chunk's
-  //    partial (ordered before it by the barrier) and, for the last arriver,
-  //    acquires every other chunk's.
-  //    Only the nch chunks that reach p_b arrive: the last of them also adds
-  //    the nchunk - nch empty chunks' share, so the counter still advances by
-  //    nchunk per step.
-  const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
-  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
-  if (cw == 0 && lane == 0) {
-    uint32_t *ctr = P.ctr + (size_t)in.sig_ctr * kCtrStride;
-    const uint32_t old = atom_add_acq_rel(ctr, 1u);
-    const bool last = old == epoch * in.nchunk + (uint32_t)nch - 1u;
-    if (last && (uint32_t)nch < in.nchunk) red_add(ctr, in.nchunk - (uint32_t)nch);
-    S.misc[2] = last ? 1 : 0;
-  }
-  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
-  if (S.misc[2]) {
-    const int PS = 2 * QPG + QPG * D;
-    const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
-    // up to MB chunks' partials in flight at once (one round trip to L2 for
-    // a group of up to MB chunks); per batch, the batch's maximum first, then
-    // one rescale of the running sums
-    constexpr int MB = 16;
-    for (int o = cw * 32 + lane; o < QPG * D; o += kComputeWarps * 32) {
-      const int h = o / D;
-      float M = -INFINITY, den = 0.f, num = 0.f;
-      for (int c0 = 0; c0 < nch; c0 += MB) {
-        float mc[MB], lc[MB], oc[MB];
-#pragma unroll
-        for (int u = 0; u < MB; ++u) {
-          mc[u] = -INFINITY;
-          lc[u] = oc[u] = 0.f;
-          if (c0 + u < nch) {
-            const float *pc = pb + (size_t)(c0 + u) * PS;
-            mc[u] = __ldcg(pc + h);
-            lc[u] = __ldcg(pc + QPG + h);
-            oc[u] = __ldcg(pc + 2 * QPG + o);
-          }
-        }
-        float Mb = M;
-#pragma unroll
-        for (int u = 0; u < MB; ++u) Mb = fmaxf(Mb, mc[u]);
-        if (Mb == -INFINITY) continue;
-        const float a = __expf(M - Mb);
-        den *= a;
-        num *= a;
-#pragma unroll
-        for (int u = 0; u < MB; ++u) {
-          if (mc[u] == -INFINITY) continue;
-          const float w = __expf(mc[u] - Mb);
-          den = fmaf(w, lc[u], den);
-          num = fmaf(w, oc[u], num);
-        }
-        M = Mb;
-      }
-      P.attn[(size_t)b * P.nq * D + (size_t)g * QPG * D + o] = num / den;
-    }
-    if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
-    if (cw == 0 && lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
-  }
-  return true;
+  // 6. arrival, and the group merge by its last chunk
+  return attn_arrive_merge<D, QPG>(P, S, in, cw, lane, att_uses, epoch, b, g, pos);
 }
 
+// The same chunk for tensor-core plans with d = 64 and at most four query
+// heads per group: the chunk's positions are split over all compute warps,
+// and each warp scores its rows for every head of the group, so every key
+// and value row is read from shared memory once (by one warp) instead of
+// once per head, and every warp has the same number of rows.  Scores are
+// kept as [row][head]; the per-warp partials {o[head][d]}, {m, l}[head] are
+// single-buffered: the per-head merge reads them before the barrier that
+// precedes the arrival, which every warp passes before it can reach the next
+// chunk.
+template <int QPG>
+__device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, const mk_instr &in,
+                                            const SlotMeta &meta, int cw, int lane,
+                                            uint32_t &att_uses, uint32_t epoch) {
+  constexpr int D = 64;
+  constexpr int LPP = D / 8;      // lanes per key row (16 bytes each)
+  constexpr int RPS = 32 / LPP;   // key rows per warp step
+  constexpr int DPL = D / 32;     // value dims per lane
+  const int b = in.b, g = in.g, pos = S.pos[b];
+  int p0, p1;
+  attn_range(P, pos, in.chunk, p0, p1);
+  const int n_tot = p1 - p0;
+  const int n_old = max(0, min(p1, pos) - p0);  // rows that come from the ring
+  const uint32_t E = P.ring_pages;
+  const int len = (n_tot + kComputeWarps - 1) / kComputeWarps;
+  const int j0 = min(cw * len, n_tot), j1 = min(j0 + len, n_tot);
+  const int part = lane % LPP;
+  const bool stamp = cw == 0 && lane == 0 && (P.flags & MK_FLAG_TRACE);
+  SlotMeta &mw = const_cast<SlotMeta &>(meta);  // this entry's slot in shared memory
+  if (n_tot <= 0) return true;
+  float *op = S.opart;                                  // [warp][head][D]
+  float *mlp = op + kComputeWarps * QPG * D;            // [warp][head][m, l]
+  float *sw = mlp + kComputeWarps * QPG * 2 + (size_t)cw * P.att_lmax;  // [row][head]
+
+  // queries of every head (8 dims per lane), pre-scaled; the current
+  // position's key slice and value dims if this warp covers p_b
+  float q8[QPG][8], kn8[8], vn[DPL];
+  {
+    const float sc = P.attn_scale;
+#pragma unroll
+    for (int h = 0; h < QPG; ++h) {
+      const float *qh = P.q + ((size_t)b * P.nq + (size_t)g * QPG + h) * D + part * 8;
+      const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(qh));
+      const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(qh + 4));
+      q8[h][0] = x0.x * sc; q8[h][1] = x0.y * sc; q8[h][2] = x0.z * sc; q8[h][3] = x0.w * sc;
+      q8[h][4] = x1.x * sc; q8[h][5] = x1.y * sc; q8[h][6] = x1.z * sc; q8[h][7] = x1.w * sc;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) kn8[u] = 0.f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) vn[k] = 0.f;
+    if (n_old >= j0 && n_old < j1) {
+      const size_t at = kv_row(P, in.layer, b, g, pos);
+      const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(P.kc + at + part * 8));
+      kn8[0] = bf_lo(w.x); kn8[1] = bf_hi(w.x); kn8[2] = bf_lo(w.y); kn8[3] = bf_hi(w.y);
+      kn8[4] = bf_lo(w.z); kn8[5] = bf_hi(w.z); kn8[6] = bf_lo(w.w); kn8[7] = bf_hi(w.w);
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) vn[k] = bf1(__ldcg(P.vc + at + lane * DPL + k));
+    }
+  }
+  if (stamp) mw.t_input = gtimer();
+  const bool paged = n_old > 0;  // one key page and one value page
+  const uint8_t *__restrict__ kpage = S.ring + (size_t)(meta.seq0 % E) * P.page_bytes;
+  const uint8_t *__restrict__ vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
+  if (paged && !warp_wait(P, S, &S.full[meta.seq0 % E], (meta.seq0 / E) & 1u, kWhereCompute | meta.idx))
+    return false;
+
+  // 1. scores of rows j0..j1 for every head: a block of LPP steps covers 32
+  //    rows; per head one transposing butterfly over the LPP lanes of a row
+  //    group leaves lane `part` with the full score of step `part`.  Steps t
+  //    and t + LPP/2 are scored together and take the butterfly's first level
+  //    at once, so only half the steps' partial sums are live per head.
+  auto score8 = [&](int j, float (&out)[QPG]) {
+    float k8[8];
+    if (j < n_old) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(kpage + (size_t)j * D * 2 + part * 16);
+      k8[0] = bf_lo(w.x); k8[1] = bf_hi(w.x); k8[2] = bf_lo(w.y); k8[3] = bf_hi(w.y);
+      k8[4] = bf_lo(w.z); k8[5] = bf_hi(w.z); k8[6] = bf_lo(w.w); k8[7] = bf_hi(w.w);
+    } else {
+      const bool cur = j < j1;  // the row of p_b itself
+#pragma unroll
+      for (int u = 0; u < 8; ++u) k8[u] = cur ? kn8[u] : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < QPG; ++h) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        a0 = fmaf(q8[h][u], k8[u], a0);
+        a1 = fmaf(q8[h][u + 1], k8[u + 1], a1);
+      }
+      out[h] = a0 + a1;
+    }
+  };
+  constexpr int HALF = LPP / 2;
+  for (int jb = j0; jb < j1; jb += LPP * RPS) {
+    float v[QPG][HALF];
+    const bool up4 = (part & HALF) != 0;
+#pragma unroll
+    for (int t = 0; t < HALF; ++t) {
+      float va[QPG], vb[QPG];
+      score8(jb + t * RPS + lane / LPP, va);
+      score8(jb + (t + HALF) * RPS + lane / LPP, vb);
+#pragma unroll
+      for (int h = 0; h < QPG; ++h) {
+        const float send = up4 ? va[h] : vb[h];
+        const float keep = up4 ? vb[h] : va[h];
+        v[h][t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, HALF);
+      }
+    }
+#pragma unroll
+    for (int hw = HALF / 2; hw >= 1; hw /= 2) {
+      const bool upper = (part & hw) != 0;
+#pragma unroll
+      for (int h = 0; h < QPG; ++h)
+#pragma unroll
+        for (int i = 0; i < hw; ++i) {
+          const float send = upper ? v[h][i] : v[h][i + hw];
+          const float keep = upper ? v[h][i + hw] : v[h][i];
+          v[h][i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, hw);
+        }
+    }
+    const int jr = jb + part * RPS + lane / LPP;
+    if (jr < j1)
+#pragma unroll
+      for (int h = 0; h < QPG; ++h) sw[(jr - j0) * QPG + h] = v[h][0];
+  }
+  __syncwarp();
+  if (stamp) mw.t_page0 = gtimer();
+
+  // 2. per head: this warp's maximum, probabilities and denominator
+  const int cnt = j1 - j0;  // at most 32 rows per warp (chunks of <= 448 positions)
+  float m[QPG], l[QPG];
+#pragma unroll
+  for (int h = 0; h < QPG; ++h) {
+    const float s = lane < cnt ? sw[lane * QPG + h] : -INFINITY;
+    m[h] = warp_max(s);
+    const float pj = lane < cnt ? __expf(s - m[h]) : 0.f;
+    if (lane < cnt) sw[lane * QPG + h] = pj;
+    l[h] = warp_sum(pj);
+  }
+  __syncwarp();
+
+  // 3. o[h] = sum_j p_j[h] v_j over this warp's rows; lanes own DPL dims,
+  //    even and odd rows in separate accumulators
+  if (paged && !warp_wait(P, S, &S.full[(meta.seq0 + 1) % E], ((meta.seq0 + 1) / E) & 1u,
+                          kWhereCompute | meta.idx))
+    return false;
+  if (stamp) mw.t_pagel = gtimer();
+  float o[2][QPG][DPL];
+#pragma unroll
+  for (int e = 0; e < 2; ++e)
+#pragma unroll
+    for (int h = 0; h < QPG; ++h)
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[e][h][k] = 0.f;
+  const uint8_t *__restrict__ vrow = vpage + lane * DPL * 2;
+  for (int j = j0; j < j1; j += 2) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int jj = j + e;
+      if (jj < j1) {
+        float vv[DPL];
+        if (jj < n_old) {
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow + (size_t)jj * D * 2);
+          vv[0] = bf_lo(w);
+          vv[1] = bf_hi(w);
+        } else {
+#pragma unroll
+          for (int k = 0; k < DPL; ++k) vv[k] = vn[k];
+        }
+        float pj[QPG];
+        if constexpr (QPG == 4) {
+          const float4 p4 = *reinterpret_cast<const float4 *>(sw + (jj - j0) * QPG);
+          pj[0] = p4.x; pj[1] = p4.y; pj[2] = p4.z; pj[3] = p4.w;
+        } else {
+#pragma unroll
+          for (int h = 0; h < QPG; ++h) pj[h] = sw[(jj - j0) * QPG + h];
+        }
+#pragma unroll
+        for (int h = 0; h < QPG; ++h)
+#pragma unroll
+          for (int k = 0; k < DPL; ++k) o[e][h][k] = fmaf(pj[h], vv[k], o[e][h][k]);
+      }
+    }
+  }
+
+  // 4. per-warp partials, then one block barrier
+#pragma unroll
+  for (int h = 0; h < QPG; ++h) {
+#pragma unroll
+    for (int k = 0; k < DPL; ++k)
+      op[((size_t)cw * QPG + h) * D + lane * DPL + k] = o[0][h][k] + o[1][h][k];
+    if (lane == 0) {
+      mlp[(cw * QPG + h) * 2] = cnt > 0 ? m[h] : -INFINITY;
+      mlp[(cw * QPG + h) * 2 + 1] = l[h];
+    }
+  }
+  if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
+  if (paged && cw == 0 && lane == 0) {  // every warp is past the pages
+    mbar_arrive(&S.empty[meta.seq0 % E]);
+    mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
+  }
+
+  // 5. warp hh < QPG merges the partials of head hh into the chunk partial
+  if (cw < QPG) {
+    float M = -INFINITY;
+    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, mlp[(w * QPG + cw) * 2]);
+    float L = 0.f, acc[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[k] = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kComputeWarps; ++w) {
+        const float mw_ = mlp[(w * QPG + cw) * 2];
+        if (mw_ == -INFINITY) continue;
+        const float a = __expf(mw_ - M);
+        L = fmaf(a, mlp[(w * QPG + cw) * 2 + 1], L);
+#pragma unroll
+        for (int k = 0; k < DPL; ++k)
+          acc[k] = fmaf(a, op[((size_t)w * QPG + cw) * D + lane * DPL + k], acc[k]);
+      }
+    }
+    const int PS = 2 * QPG + QPG * D;
+    float *dst = P.part + (((size_t)b * P.nkv + g) * P.nchunk + in.chunk) * PS;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) dst[2 * QPG + cw * D + lane * DPL + k] = acc[k];
+    if (lane == 0) {
+      dst[cw] = M;
+      dst[QPG + cw] = L;
+    }
+  }
+
+  // 6. arrival, and the group merge by its last chunk
+  return attn_arrive_merge<D, QPG>(P, S, in, cw, lane, att_uses, epoch, b, g, pos);
+}
+
+template <bool TC>
 DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
                         const SlotMeta &meta, int cw, int lane, uint32_t &att_uses,
                         uint32_t epoch) {
+  if constexpr (TC) {
+    if (P.att_grp) {
+      switch (P.qpg) {
+        case 1: return attn_chunk_grp<1>(P, S, in, meta, cw, lane, att_uses, epoch);
+        case 2: return attn_chunk_grp<2>(P, S, in, meta, cw, lane, att_uses, epoch);
+        default: return attn_chunk_grp<4>(P, S, in, meta, cw, lane, att_uses, epoch);
+      }
+    }
+  }
   if (P.d == 64) {
     switch (P.qpg) {
       case 1: return attn_chunk<64, 1>(P, S, in, meta, cw, lane, att_uses, epoch);
@@ -1168,7 +1425,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return;
     bool ok;
     if (in.op == MK_OP_ATTN) {
-      ok = attn_dispatch(P, S, in, meta, cw, lane, att_uses, epoch);
+      ok = attn_dispatch<TC>(P, S, in, meta, cw, lane, att_uses, epoch);
       xkey = 0xFFFFFFFFu;
     } else if (TC) {
       ok = gemv_tc(P, S, in, meta, cw, lane, epoch, xkey, xbar_uses, key_changes, tc_uses,

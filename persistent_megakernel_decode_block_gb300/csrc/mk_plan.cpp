@@ -207,8 +207,14 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.attn_chunk = ch;
   P.nchunk = cdiv(c.max_ctx, ch);
   // each compute warp keeps the scores of its share of a chunk; a head has
-  // at least kComputeWarps / qpg warps
-  P.att_lmax = (uint32_t)align_up(cdiv(ch, (uint32_t)(kComputeWarps / qpg)), 4);
+  // at least kComputeWarps / qpg warps.  Tensor-core plans with d = 64 and at
+  // most four heads per group split a chunk's positions over all compute
+  // warps instead, each warp scoring its rows for every head of the group
+  // (one read of each key and value row per warp): scores [row][head].
+  P.att_grp = P.tc && d == 64 && qpg <= 4;
+  P.att_lmax = P.att_grp
+                   ? (uint32_t)align_up((uint64_t)cdiv(ch, (uint32_t)kComputeWarps) * qpg, 4)
+                   : (uint32_t)align_up(cdiv(ch, (uint32_t)(kComputeWarps / qpg)), 4);
 
   // ---- shared-memory layout -------------------------------------------------
   // per-slot dot products (items x batch); also the size of the storer's residual buffer
@@ -227,6 +233,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // attention: per-warp partials {o[d]} and {m, l}, double-buffered, then
   // per-warp scores
   uint32_t att_bytes = (2 * kComputeWarps * d + 2 * kComputeWarps * 2 + kComputeWarps * P.att_lmax) * 4;
+  // grouped attention: per-warp partials {o[qpg][d]} and {m, l}[qpg], single-buffered
+  if (P.att_grp)
+    att_bytes = (uint32_t)(kComputeWarps * qpg * (d + 2) + kComputeWarps * P.att_lmax) * 4;
   // tensor-core plans also gather a split block's slice sums here (MR x B)
   if (P.tc) att_bytes = std::max<uint32_t>(att_bytes, 128u * (uint32_t)B * 4u);
   uint32_t rel_att = take(att_bytes, 16);
