@@ -42,7 +42,7 @@ def args_():
     p.add_argument("--impl", default="mine", choices=["mine", "reference"])
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--sched", default="static", choices=["dynamic", "static"])
+    p.add_argument("--sched", default="static", choices=["dynamic", "static", "hybrid"])
     p.add_argument("--l2kb", type=int, default=0,
                    help="mk_config.l2_prefetch_kb: KB per block prefetched into L2 ahead of the ring")
     p.add_argument("--stream", action="store_true",
@@ -338,8 +338,9 @@ def run_mine(a):
     def up(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev)
 
-    cfg = mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC if a.sched == "static"
-                         else mk.MK_SCHED_DYNAMIC,
+    cfg = mk.make_config(m, B, mctx, sched_mode={"static": mk.MK_SCHED_STATIC,
+                                                 "hybrid": mk.MK_SCHED_HYBRID,
+                                                 "dynamic": mk.MK_SCHED_DYNAMIC}[a.sched],
                          flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_STREAM_B1 if a.stream else 0),
                          l2_prefetch_kb=a.l2kb)
     plan = mk.mk_plan(cfg)

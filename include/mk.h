@@ -76,6 +76,12 @@ extern "C" {
 
 #define MK_SCHED_DYNAMIC 0 /* global work queue, one atomic claim per instruction */
 #define MK_SCHED_STATIC 1  /* per-SM lists, round-robin over the queue order */
+#define MK_SCHED_HYBRID 2  /* per-SM lists for the projections; each layer's attention
+                              chunks claimed from that layer's own queue, one claim at
+                              a time as a block's instruction FIFO drains (the pages'
+                              hybrid of static and dynamic scheduling, « 2 · Définition
+                              et généalogie », §2.6 "5. L'ordonnancement"); not with
+                              MK_FLAG_STREAM_B1 */
 
 /* Model shape and plan options.  A plan is built for one batch size
    (« Résumé exécutif », "Où en est-on en 2026": a megakernel is rebuilt per
@@ -86,7 +92,7 @@ typedef struct mk_config {
   int32_t tie_embeddings;  /* 1: the LM head is the embedding matrix */
   int32_t batch;           /* sequences per step, 1..16 */
   int32_t max_ctx;         /* KV capacity per sequence (positions), multiple of 16 */
-  int32_t sched_mode;      /* MK_SCHED_DYNAMIC or MK_SCHED_STATIC */
+  int32_t sched_mode;      /* MK_SCHED_DYNAMIC, MK_SCHED_STATIC or MK_SCHED_HYBRID */
   uint32_t flags;          /* MK_FLAG_* */
   int32_t wait_timeout_us; /* device-side wait limit; 0 -> 1,000,000 */
   int32_t num_sms;         /* 0 -> query the device; >0 overrides (host-only planning) */
@@ -216,7 +222,11 @@ MK_API int mk_plan_tables(mk_plan_t plan, const mk_instr **instr, size_t *n_inst
                           const uint32_t **counter_inc, size_t *n_counters);
 
 /* Phase table (queue order) and static per-SM lists: list s holds
-   list_idx[list_off[s] .. list_off[s+1]); n_lists = n_blocks. */
+   list_idx[list_off[s] .. list_off[s+1]); n_lists = n_blocks.  In
+   MK_SCHED_HYBRID plans every list holds, in place of layer l's attention
+   instructions, one entry MK_LIST_ATTN | l: there the block claims chunks
+   from layer l's attention queue until it is empty. */
+#define MK_LIST_ATTN 0x80000000u
 MK_API int mk_plan_phases(mk_plan_t plan, const mk_phase **phases, size_t *n_phases);
 MK_API int mk_plan_lists(mk_plan_t plan, const uint32_t **list_off, const uint32_t **list_idx,
                          size_t *n_lists);

@@ -55,7 +55,8 @@ def lib():
             "or_decode_step": (i, [ctypes.POINTER(_Model), i, i, vp, vp, vp, vp, vp]),
             "or_replay": (i, [vp, i, i, ctypes.POINTER(_Shape), i, vp, vp, vp,
                               ctypes.c_char_p, i]),
-            "or_simulate": (i, [vp, i, i, i, i, ctypes.c_uint64, i, vp, vp, ctypes.c_char_p, i]),
+            "or_simulate": (i, [vp, i, i, i, i, ctypes.c_uint64, i, vp, vp, vp, i, i,
+                                ctypes.c_char_p, i]),
             "or_explore": (ctypes.c_long, [vp, i, i, i, ctypes.c_long, ctypes.c_char_p, i]),
             "or_redeal": (i, [vp, i, ctypes.POINTER(_Shape), i, vp, vp, i, vp, ctypes.c_char_p,
                               i]),
@@ -184,14 +185,20 @@ def replay(table, n_instr, n_counters, cfg, batch, n_sms, list_off=None, list_id
 
 
 def simulate(table, n_instr, n_counters, n_sms, fifo_depth, seed=0, trials=4, list_off=None,
-             list_idx=None):
+             list_idx=None, att_first=None, att_count=0):
+    """Seeded random interleavings of n_sms virtual SMs (dynamic queue, static
+    lists, or hybrid lists whose marker entries claim from per-layer attention
+    queues: att_first[l] + 0 .. att_count - 1).  Raises on a deadlock."""
     table = np.ascontiguousarray(table, dtype=np.uint8)
     msg = ctypes.create_string_buffer(512)
     lo = None if list_off is None else np.ascontiguousarray(list_off, dtype=np.uint32)
     li = None if list_idx is None else np.ascontiguousarray(list_idx, dtype=np.uint32)
+    af = None if att_first is None else np.ascontiguousarray(att_first, dtype=np.uint32)
     rc = lib().or_simulate(table.ctypes.data, n_instr, n_counters, n_sms, fifo_depth, seed,
                            trials, None if lo is None else lo.ctypes.data,
-                           None if li is None else li.ctypes.data, msg, 512)
+                           None if li is None else li.ctypes.data,
+                           None if af is None else af.ctypes.data,
+                           0 if af is None else af.size, int(att_count), msg, 512)
     if rc != 0:
         raise AssertionError("simulate: " + msg.value.decode())
 

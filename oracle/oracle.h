@@ -34,7 +34,7 @@ int or_replay(const void *table, int n_instr, int n_counters, const or_shape *s,
               int msg_len);
 int or_simulate(const void *table, int n_instr, int n_counters, int S, int fifo_depth,
                 uint64_t seed, int trials, const uint32_t *list_off, const uint32_t *list_idx,
-                char *msg, int msg_len);
+                const uint32_t *att_first, int n_att, int att_count, char *msg, int msg_len);
 long or_explore(const void *table, int n_instr, int n_counters, int fifo_depth, long max_states,
                 char *msg, int msg_len);
 int or_redeal(const void *table, int n_instr, const or_shape *s, int attn_chunk,

@@ -486,9 +486,12 @@ out:
  * Virtual SMs each hold a FIFO of claimed instructions (depth fifo_depth) and
  * finish them in claim order; an instruction can finish once its counter has
  * reached its target.  Dynamic mode claims the next queue entry; static mode
- * takes the next entry of the SM's own list.  Every step picks one enabled
- * action at random (seeded); finding no enabled action with work left is a
- * deadlock. */
+ * takes the next entry of the SM's own list.  Hybrid lists (att_first not
+ * NULL) hold, in place of layer l's attention instructions, one entry with
+ * bit 31 set and l below it: there the SM claims att_first[l] + q[l]++ from
+ * that layer's queue until all att_count are claimed, then goes on with its
+ * list.  Every step picks one enabled action at random (seeded); finding no
+ * enabled action with work left is a deadlock. */
 static uint64_t rng_next(uint64_t *s) {
   uint64_t z = (*s += 0x9E3779B97F4A7C15ULL);
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
@@ -505,8 +508,11 @@ static int ready(const rec_t *r, const uint32_t *cnt) {
   return r->wait_ctr == NONE || cnt[r->wait_ctr] >= r->wait_tgt;
 }
 
+#define ATT_MARK 0x80000000u
+
 int or_simulate(const void *table, int N, int n_ctr, int S, int D, uint64_t seed, int trials,
-                const uint32_t *list_off, const uint32_t *list_idx, char *msg, int msg_len) {
+                const uint32_t *list_off, const uint32_t *list_idx, const uint32_t *att_first,
+                int n_att, int att_count, char *msg, int msg_len) {
   if (S <= 0 || D <= 0 || N <= 0) return fail(msg, msg_len, "bad arguments");
   rec_t *r = (rec_t *)malloc(sizeof(rec_t) * (size_t)N);
   for (int i = 0; i < N; ++i) decode(table, i, &r[i]);
@@ -515,6 +521,9 @@ int or_simulate(const void *table, int N, int n_ctr, int S, int D, uint64_t seed
   int *fh = (int *)malloc(sizeof(int) * (size_t)S), *fl = (int *)malloc(sizeof(int) * (size_t)S);
   uint32_t *lp = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)S);
   int *acts = (int *)malloc(sizeof(int) * (size_t)2 * S);
+  int *att_l = (int *)malloc(sizeof(int) * (size_t)S);       /* hybrid: layer being claimed */
+  int *aq = (int *)calloc((size_t)(n_att > 0 ? n_att : 1), sizeof(int));
+  unsigned char *seen = (unsigned char *)malloc((size_t)N);
   int rc = 0;
   for (int t = 0; t < trials && rc == 0; ++t) {
     uint64_t st = seed * 1000003ULL + (uint64_t)t;
@@ -522,15 +531,33 @@ int or_simulate(const void *table, int N, int n_ctr, int S, int D, uint64_t seed
     for (int s = 0; s < S; ++s) {
       fh[s] = fl[s] = 0;
       lp[s] = list_off ? list_off[s] : 0;
+      att_l[s] = -1;
     }
+    for (int l = 0; l < n_att; ++l) aq[l] = 0;
+    memset(seen, 0, (size_t)N);
     int nx = 0, done = 0;
     while (done < N) {
       int na = 0;
       for (int s = 0; s < S; ++s) {
-        int can_claim = fl[s] < D && (list_off ? lp[s] < list_off[s + 1] : nx < N);
+        /* hybrid: step over exhausted queues and onto markers until a claim
+           is possible or the list ends (no instruction is taken here) */
+        while (att_first && list_off) {
+          if (att_l[s] >= 0 && aq[att_l[s]] < att_count) break;
+          att_l[s] = -1;
+          if (lp[s] >= list_off[s + 1] || !(list_idx[lp[s]] & ATT_MARK)) break;
+          const uint32_t l = list_idx[lp[s]++] & ~ATT_MARK;
+          if ((int)l >= n_att) {
+            rc = fail(msg, msg_len, "list marker for layer %u of %d", l, n_att);
+            break;
+          }
+          att_l[s] = (int)l;
+        }
+        if (rc) break;
+        int can_claim = fl[s] < D && (att_l[s] >= 0 || (list_off ? lp[s] < list_off[s + 1] : nx < N));
         if (can_claim) acts[na++] = 2 * s;
         if (fl[s] > 0 && ready(&r[fifo[s * D + fh[s]]], cnt)) acts[na++] = 2 * s + 1;
       }
+      if (rc) break;
       if (na == 0) {
         rc = fail(msg, msg_len, "deadlock in trial %d with %d of %d done", t, done, N);
         break;
@@ -543,7 +570,13 @@ int or_simulate(const void *table, int N, int n_ctr, int S, int D, uint64_t seed
         apply_done(&r[x], cnt);
         done++;
       } else {
-        int x = list_off ? (int)list_idx[lp[s]++] : nx++;
+        int x;
+        if (att_l[s] >= 0) x = (int)att_first[att_l[s]] + aq[att_l[s]]++;
+        else x = list_off ? (int)list_idx[lp[s]++] : nx++;
+        if (x < 0 || x >= N || seen[x]++) {
+          rc = fail(msg, msg_len, "instruction %d out of range or claimed twice", x);
+          break;
+        }
         fifo[s * D + (fh[s] + fl[s]) % D] = x;
         fl[s]++;
       }
@@ -556,6 +589,9 @@ int or_simulate(const void *table, int N, int n_ctr, int S, int D, uint64_t seed
   free(fl);
   free(lp);
   free(acts);
+  free(att_l);
+  free(aq);
+  free(seen);
   return rc;
 }
 

@@ -35,7 +35,7 @@ constexpr int kCtlStatus = 0, kCtlWhere = 1, kCtlAbort = 2, kCtlEpoch = 3;
 constexpr int kCtlExit = 32, kCtlQueue = 64, kCtlWords = 96;
 
 // run modes
-constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2;
+constexpr int kModeDynamic = 0, kModeStatic = 1, kModeRange = 2, kModeHybrid = 3;
 
 // GEMV geometry of one op: K input columns split into NS slices of SW
 // columns; an item = one weight row restricted to one slice (2*SW bytes);
@@ -54,6 +54,9 @@ struct KParams {
   const mk_instr *instr;
   uint32_t n_instr;
   const uint32_t *list_off, *list_idx;
+  uint32_t *aq;                // hybrid: per-layer attention queue (claims, epoch relative)
+  const uint32_t *att_first;   // hybrid: per layer, first instruction of its attention phase
+  uint32_t att_count;          // attention instructions per layer
   uint32_t *ctr, *ctrl, *exec;
   const uint32_t *ctr_inc;  // signals per step of every counter
   unsigned long long *trace;

@@ -145,13 +145,16 @@ DEVI uint32_t balance_attn(const KParams &P, const Smem &S, mk_instr &in, uint32
   return idx - (uint32_t)j + (uint32_t)jn;
 }
 
-template <bool TC>
+// HYB: the hybrid schedule's claims and publish gate (compiled only into the
+// loader that runs hybrid plans, so the others' polling loop stays as short)
+template <bool TC, bool HYB>
 DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   const uint64_t pol = policy_evict_first();
   const uint32_t N = P.n_instr, E = P.ring_pages, PG = P.page_bytes;
   const uint32_t qbase = epoch * (N + P.n_blocks);
   uint32_t list_k = 0, list_end = 0, range_taken = 0;
-  if (P.mode == kModeStatic) {
+  int att_l = -1;  // hybrid: the layer whose attention queue this block claims from
+  if (P.mode == kModeStatic || P.mode == kModeHybrid) {
     list_k = P.list_off[blockIdx.x];
     list_end = P.list_off[blockIdx.x + 1];
   }
@@ -160,6 +163,21 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   auto claim = [&]() -> uint32_t {
     if (P.mode == kModeDynamic) return atomicAdd(P.ctrl + kCtlQueue, 1u) - qbase;
     if (P.mode == kModeStatic) return list_k < list_end ? __ldg(P.list_idx + list_k++) : N;
+    if (HYB) {
+      // the list, where an attention marker hands over to that layer's queue
+      // until it is empty (every block takes one failing claim per layer)
+      while (true) {
+        if (att_l >= 0) {
+          const uint32_t j = atomicAdd(P.aq + att_l, 1u) - epoch * (P.att_count + P.n_blocks);
+          if (j < P.att_count) return __ldg(P.att_first + att_l) + j;
+          att_l = -1;
+        }
+        if (list_k >= list_end) return N;
+        const uint32_t e = __ldg(P.list_idx + list_k++);
+        if (!(e & MK_LIST_ATTN)) return e;
+        att_l = (int)(e & ~MK_LIST_ATTN);
+      }
+    }
     const uint32_t r = range_taken ? N : P.range_first + blockIdx.x;
     range_taken = 1;
     return r;
@@ -181,7 +199,13 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
   while (true) {
     bool progress = false;
     // ---- claim cursor
-    if (!ended && fs_c - fs_s < P.lookahead) {
+    // hybrid: an attention chunk claimed from a queue is published only once
+    // the compute warps have started the entry before it, so a block takes
+    // chunks as it drains them, not as fast as its loader runs ahead
+    const bool gate = HYB && a < N && (ra[0].x & 0xFFu) == MK_OP_ATTN &&
+                      fs_c > 0 &&
+                      !mbar_test(&S.rdy[(fs_c - 1) % kFifo], ((fs_c - 1) / kFifo) & 1u);
+    if (!ended && !gate && fs_c - fs_s < P.lookahead) {
       const uint32_t f = fs_c % kFifo, k = fs_c / kFifo;
       if (k == 0 || mbar_test(&S.iempty[f], (k - 1) & 1u)) {
         if (a >= N) {
@@ -195,7 +219,8 @@ DEVI void loader(const KParams &P, const Smem &S, uint32_t epoch) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = ra[i];
           uint32_t idx = a;
-          if (TC && P.mode == kModeStatic && S.fifo[f].op == MK_OP_ATTN)  // (batch > 1)
+          if (TC && (P.mode == kModeStatic || HYB) &&
+              S.fifo[f].op == MK_OP_ATTN)  // (batch > 1)
             idx = balance_attn(P, S, S.fifo[f], a);
           const mk_instr &in = S.fifo[f];
           const uint32_t np = n_pages(P, S, in);
@@ -1541,7 +1566,10 @@ DEVI void megakernel_body(const KParams &P) {
     tc_fence_after();
   }
   if (warp == 0) {
-    if (lane == 0) loader<TC>(P, S, epoch);
+    if (lane == 0) {
+      if (P.mode == kModeHybrid) loader<TC, true>(P, S, epoch);
+      else loader<TC, false>(P, S, epoch);
+    }
     __syncwarp();
   } else if (warp == 1) {
     storer(P, S, epoch, lane);

@@ -54,7 +54,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   if (c.batch < 1 || c.batch > kMaxBatch) REJECT("batch must be in 1..16");
   if (c.max_ctx < 16 || c.max_ctx % 16) REJECT("max_ctx must be a positive multiple of 16");
   if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) REJECT("rms_eps >= 0 and rope_theta > 0 required");
-  if (c.sched_mode != MK_SCHED_DYNAMIC && c.sched_mode != MK_SCHED_STATIC) REJECT("bad sched_mode");
+  if (c.sched_mode != MK_SCHED_DYNAMIC && c.sched_mode != MK_SCHED_STATIC &&
+      c.sched_mode != MK_SCHED_HYBRID)
+    REJECT("bad sched_mode");
   if (num_sms < 1 || num_sms > 1024) REJECT("number of SMs out of range");
   const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : 32768u;
   if (page < 4096 || page > 65536 || page % 1024) REJECT("page_bytes must be a multiple of 1024 in 4096..65536");
@@ -523,12 +525,38 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   }
 
   // ---- static per-SM lists: round-robin over the queue order -------------
-  P.list_off.assign(num_sms + 1, 0);
-  for (uint32_t s = 0; s < num_sms; ++s)
-    P.list_off[s + 1] = P.list_off[s] + (uint32_t)((P.instr.size() + num_sms - 1 - s) / num_sms);
-  P.list_idx.resize(P.instr.size());
-  for (uint32_t s = 0, k = 0; s < num_sms; ++s)
-    for (size_t i = s; i < P.instr.size(); i += num_sms) P.list_idx[k++] = (uint32_t)i;
+  // Hybrid: the projections (and the LM head) are dealt round-robin as in
+  // static lists; each attention phase becomes one marker entry in every
+  // list, where the block claims from that layer's attention queue.
+  P.att_first.assign(L, 0);
+  for (const mk_phase &ph : P.phases)
+    if (ph.op == MK_OP_ATTN) P.att_first[ph.layer] = ph.first;
+  P.att_count = P.nchunk * (uint32_t)B * (uint32_t)nkv;
+  if (c.sched_mode == MK_SCHED_HYBRID) {
+    if (P.stream) REJECT("the hybrid schedule does not run the per-warp stream kernel");
+    std::vector<std::vector<uint32_t>> lists(num_sms);
+    uint32_t k = 0;
+    for (const mk_phase &ph : P.phases) {
+      if (ph.op == MK_OP_ATTN) {
+        for (auto &li : lists) li.push_back(MK_LIST_ATTN | ph.layer);
+        continue;
+      }
+      for (uint32_t i = ph.first; i < ph.first + ph.count; ++i) lists[k++ % num_sms].push_back(i);
+    }
+    P.list_off.assign(num_sms + 1, 0);
+    P.list_idx.clear();
+    for (uint32_t s = 0; s < num_sms; ++s) {
+      P.list_idx.insert(P.list_idx.end(), lists[s].begin(), lists[s].end());
+      P.list_off[s + 1] = (uint32_t)P.list_idx.size();
+    }
+  } else {
+    P.list_off.assign(num_sms + 1, 0);
+    for (uint32_t s = 0; s < num_sms; ++s)
+      P.list_off[s + 1] = P.list_off[s] + (uint32_t)((P.instr.size() + num_sms - 1 - s) / num_sms);
+    P.list_idx.resize(P.instr.size());
+    for (uint32_t s = 0, k = 0; s < num_sms; ++s)
+      for (size_t i = s; i < P.instr.size(); i += num_sms) P.list_idx[k++] = (uint32_t)i;
+  }
 
   // ---- re-tiling maps ----------------------------------------------------
   P.qkv_map.resize((size_t)(nq + 2 * nkv) * d);

@@ -15,6 +15,8 @@ struct HostPlan {
   std::vector<mk_instr> instr;
   std::vector<uint32_t> ctr_inc;
   std::vector<mk_phase> phases;
+  std::vector<uint32_t> att_first;  // per layer: first instruction of its attention phase
+  uint32_t att_count = 0;           // attention instructions per layer
   std::vector<uint32_t> list_off, list_idx;
   std::vector<int32_t> qkv_map;  // permuted q/k/v row -> row of [Wq; Wk; Wv]
   std::vector<int32_t> gu_map;   // gate/up tile row -> row of [Wg; Wu]

@@ -20,6 +20,7 @@ struct mk_plan_s {
   int device = -1;
   uint8_t *d_arena = nullptr;
   mk_instr *d_instr = nullptr;
+  uint32_t *d_aq = nullptr;  // hybrid schedule: per-layer attention queues, first instructions
   uint32_t *d_list_off = nullptr, *d_list_idx = nullptr, *d_ctr = nullptr, *d_ctrl = nullptr,
            *d_exec = nullptr, *d_ctr_inc = nullptr;
   unsigned long long *d_trace = nullptr;
@@ -79,7 +80,7 @@ MK_API const char *mk_error_string(int code) {
 
 static void free_device(mk_plan_s *p) {
   if (p->graph) cudaGraphExecDestroy(p->graph);
-  void *ptrs[] = {p->d_arena, p->d_instr, p->d_list_off, p->d_list_idx, p->d_ctr,
+  void *ptrs[] = {p->d_aq, p->d_arena, p->d_instr, p->d_list_off, p->d_list_idx, p->d_ctr,
                   p->d_ctrl, p->d_exec, p->d_ctr_inc, p->d_trace, p->d_x,
                   p->d_q, p->d_attn, p->d_h, p->d_part, p->d_cos,
                   p->d_sin, p->d_logits_stage, p->d_tok_stage, p->d_pos_stage, p->d_qkv_map,
@@ -111,7 +112,8 @@ static int setup_device(mk_plan_s *p) {
   AL(p->d_arena, H.arena_bytes);
   AL(p->d_instr, N);
   AL(p->d_list_off, H.list_off.size());
-  AL(p->d_list_idx, N);
+  AL(p->d_list_idx, H.list_idx.size());
+  AL(p->d_aq, (size_t)2 * c.n_layers);  // attention queues, then their first instructions
   AL(p->d_ctr, (size_t)H.n_ctr * kCtrStride);
   AL(p->d_ctrl, (size_t)kCtlWords);
   AL(p->d_exec, N);
@@ -133,7 +135,10 @@ static int setup_device(mk_plan_s *p) {
 #undef AL
   CK(cudaMemcpy(p->d_instr, H.instr.data(), N * sizeof(mk_instr), cudaMemcpyHostToDevice));
   CK(cudaMemcpy(p->d_list_off, H.list_off.data(), H.list_off.size() * 4, cudaMemcpyHostToDevice));
-  CK(cudaMemcpy(p->d_list_idx, H.list_idx.data(), N * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(p->d_list_idx, H.list_idx.data(), H.list_idx.size() * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemset(p->d_aq, 0, (size_t)c.n_layers * 4));
+  CK(cudaMemcpy(p->d_aq + c.n_layers, H.att_first.data(), (size_t)c.n_layers * 4,
+                cudaMemcpyHostToDevice));
   CK(cudaMemcpy(p->d_ctr_inc, H.ctr_inc.data(), H.n_ctr * 4, cudaMemcpyHostToDevice));
   CK(cudaMemcpy(p->d_qkv_map, H.qkv_map.data(), H.qkv_map.size() * 4, cudaMemcpyHostToDevice));
   CK(cudaMemcpy(p->d_gu_map, H.gu_map.data(), H.gu_map.size() * 4, cudaMemcpyHostToDevice));
@@ -163,6 +168,9 @@ static int setup_device(mk_plan_s *p) {
   P.n_instr = (uint32_t)N;
   P.list_off = p->d_list_off;
   P.list_idx = p->d_list_idx;
+  P.aq = p->d_aq;
+  P.att_first = p->d_aq + c.n_layers;
+  P.att_count = H.att_count;
   P.ctr = p->d_ctr;
   P.ctrl = p->d_ctrl;
   P.exec = p->d_exec;
@@ -202,7 +210,9 @@ static int setup_device(mk_plan_s *p) {
   P.eps = c.rms_eps;
   P.attn_scale = (float)(1.0 / sqrt((double)d));
   P.n_wait = (int32_t)H.n_wait;
-  P.mode = c.sched_mode == MK_SCHED_STATIC ? kModeStatic : kModeDynamic;
+  P.mode = c.sched_mode == MK_SCHED_STATIC   ? kModeStatic
+           : c.sched_mode == MK_SCHED_HYBRID ? kModeHybrid
+                                             : kModeDynamic;
   P.n_blocks = H.num_sms;
   P.flags = c.flags;
   // wait limits count SM cycles; budget them at the maximum SM clock
@@ -214,7 +224,7 @@ static int setup_device(mk_plan_s *p) {
   P.timeout_cycles = (uint64_t)(c.wait_timeout_us > 0 ? c.wait_timeout_us : 1000000) * (uint64_t)clk_khz / 1000ull;
   // static lists may run a full FIFO ahead; the dynamic queue claims close
   // to need so the claims still balance the blocks
-  P.lookahead = P.mode == kModeStatic ? (uint32_t)kFifo : 3u;
+  P.lookahead = P.mode == kModeDynamic ? 3u : (uint32_t)kFifo;
   P.loader_idle_ns = 64;
   P.l2_window = c.l2_prefetch_kb > 0 ? (uint32_t)c.l2_prefetch_kb * 1024u : 0u;
   P.ring_pages = H.ring_pages;
@@ -573,6 +583,7 @@ static int reset_state(mk_plan_t p, cudaStream_t s) {
   CK(cudaMemsetAsync(p->d_ctr, 0, (size_t)p->H.n_ctr * kCtrStride * 4, s));
   CK(cudaMemsetAsync(p->d_ctrl, 0, (size_t)kCtlWords * 4, s));
   CK(cudaMemsetAsync(p->d_exec, 0, p->H.instr.size() * 4, s));
+  CK(cudaMemsetAsync(p->d_aq, 0, (size_t)p->H.cfg.n_layers * 4, s));
   CK(cudaStreamSynchronize(s));
   return MK_OK;
 }

@@ -76,9 +76,10 @@ class Setup:
                             self.info["n_blocks"])
         e = n_mega + n_multi
         ctr = (inc.astype(np.uint64) * e % 2 ** 32).astype(np.uint32)
-        # the work queue is only claimed in dynamic mode: N claims plus one
-        # past-the-end claim per block and step
-        queue = 0 if self.sched == mk.MK_SCHED_STATIC else (
+        # the global work queue is only claimed in dynamic mode: N claims plus
+        # one past-the-end claim per block and step (hybrid plans claim from
+        # per-layer attention queues instead)
+        queue = 0 if self.sched != mk.MK_SCHED_DYNAMIC else (
             n_mega * (self.info["n_instr"] + self.info["n_blocks"])) % 2 ** 32
         return ctr, queue, np.full(self.info["n_instr"], e, np.uint32), e
 

@@ -176,6 +176,38 @@ def test_redealt_schedule_is_a_partition_and_never_deadlocks(name):
         mk.mk_destroy(p)
 
 
+@pytest.mark.parametrize("name", ["tiny", "llama1b_ctx1024", "llama1b_b8_ragged"])
+def test_hybrid_lists_cover_the_queue_and_never_deadlock(name):
+    """Hybrid schedule: every projection and LM-head instruction in exactly
+    one list, in queue order; one attention marker per layer in every list,
+    in layer order; the oracle's simulation of the lists with per-layer
+    attention queues completes."""
+    w = WORKLOADS[name]
+    p = host_plan(name, n_sms=40, sched_mode=mk.MK_SCHED_HYBRID)
+    try:
+        info = mk.mk_plan_info(p)
+        rec, raw, _ = mk.mk_plan_tables(p)
+        off, idx = mk.mk_plan_lists(p)
+        L = w["model"]["n_layers"]
+        is_mark = (idx & mk.MK_LIST_ATTN) != 0
+        plain = idx[~is_mark]
+        want = np.nonzero(rec["op"] != mk.MK_OP_ATTN)[0]
+        assert np.array_equal(np.sort(plain), want)
+        for s_ in range(len(off) - 1):
+            li = idx[off[s_]:off[s_ + 1]]
+            m = (li & mk.MK_LIST_ATTN) != 0
+            assert np.array_equal(li[m] & ~np.uint32(mk.MK_LIST_ATTN), np.arange(L))
+            assert np.all(np.diff(li[~m].astype(np.int64)) > 0)
+        ph = mk.mk_plan_phases(p)
+        first = np.array([f for f, c, op, l in ph if op == mk.MK_OP_ATTN], np.uint32)
+        cnt = [c for f, c, op, l in ph if op == mk.MK_OP_ATTN][0]
+        oracle.simulate(raw, info["n_instr"], info["n_counters"], info["n_blocks"],
+                        info["fifo_depth"], seed=5, trials=2, list_off=off, list_idx=idx,
+                        att_first=first, att_count=cnt)
+    finally:
+        mk.mk_destroy(p)
+
+
 @pytest.mark.parametrize("name", ORDER)
 def test_attention_phase_order(name):
     """A layer's attention chunks are chunk-major (then sequence, then group)

@@ -44,7 +44,7 @@ def check_counters(s, n_mega, n_multi=0):
     assert np.array_equal(exe, want_exec)
 
 
-@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC])
+@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
 @pytest.mark.parametrize("tie", [False, True])
 def test_tiny_all_steps(sched, tie):
     s = Setup("tiny", sched=sched, tie=tie)
@@ -73,7 +73,7 @@ def test_full_size_workloads(name, steps):
         s.close()
 
 
-@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC])
+@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
 def test_tiny_batched_tensor_core_path(sched):
     """Batch > 1: every projection on tcgen05 (split along K, last slice
     reduces), all steps teacher-forced against the oracle."""
@@ -87,8 +87,9 @@ def test_tiny_batched_tensor_core_path(sched):
         s.close()
 
 
-def test_static_schedule_full_size():
-    s = Setup("llama1b_ctx1024", sched=mk.MK_SCHED_STATIC)
+@pytest.mark.parametrize("sched", [mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
+def test_static_and_hybrid_schedules_full_size(sched):
+    s = Setup("llama1b_ctx1024", sched=sched)
     try:
         teacher_forced(s, 2)
         check_counters(s, 2)

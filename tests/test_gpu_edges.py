@@ -10,8 +10,8 @@ tests, the oracle's argmax feeding both sides):
     key-page boundary (256 keys of head_dim 64 fill one 32 KB page; with
     256-position chunks a chunk is one page),
 at batch 1 (shared page ring; the opt-in per-warp stream kernel where it
-plans the same chunks) and at batch > 1 (tensor-core kernel, dynamic queue
-and static lists).  Counters, queue and execution counts stay bit-exact
+plans the same chunks) and at batch > 1 (tensor-core kernel, dynamic queue,
+static lists and the hybrid schedule).  Counters, queue and execution counts stay bit-exact
 against the oracle's replay and the KV cache the steps wrote matches the
 oracle's.
 
@@ -104,7 +104,7 @@ BATCHED = {
 
 
 @pytest.mark.parametrize("case", sorted(BATCHED))
-@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC])
+@pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
 def test_batched_edges(case, sched):
     name, ctx, mctx, steps, chunk = BATCHED[case]
     s = Setup(name, ctx=ctx, mctx=mctx, sched=sched)

@@ -221,3 +221,45 @@ def test_redeal_rejects_a_list_that_repeats_a_slot():
     idx = np.array([0, 1, 2, 3, 4, 5, 6, 7, 7, 9], np.uint32)
     with pytest.raises(AssertionError):
         oracle.redeal(t, n, RCFG, RB, RCH, (5, 20), idx)
+
+
+# ---- hybrid lists: projections dealt round-robin, attention claimed from a
+# per-layer queue (a list entry MARK | l hands over to layer l's queue)
+MARK = 0x80000000
+ATT_FIRST = [4, 18]  # the hand table: 14 records per layer, attention at 4..7
+
+
+def hybrid_lists(n_sms=2, drop_marker=False, bad_layer=False, repeat=False):
+    t, n = build()
+    rec = np.frombuffer(t.tobytes(), dtype=np.uint8).reshape(n, 64)
+    lists = [[] for _ in range(n_sms)]
+    k = 0
+    for i in range(n):
+        if rec[i, 0] == ATTN:
+            l = int(rec[i, 2])
+            if i == ATT_FIRST[l]:
+                for s, li in enumerate(lists):
+                    if not (drop_marker and l == 1):
+                        li.append(MARK | (5 if bad_layer and s == 0 else l))
+            continue
+        lists[k % n_sms].append(i)
+        k += 1
+    if repeat:
+        lists[0].append(lists[1][0])
+    off = np.cumsum([0] + [len(li) for li in lists]).astype(np.uint32)
+    idx = np.array([x for li in lists for x in li], np.uint32)
+    return t, n, off, idx
+
+
+def test_hybrid_lists_complete_in_simulation():
+    t, n, off, idx = hybrid_lists()
+    oracle.simulate(t, n, NCTR, 2, 3, seed=3, trials=20, list_off=off, list_idx=idx,
+                    att_first=ATT_FIRST, att_count=4)
+
+
+@pytest.mark.parametrize("kw", [dict(drop_marker=True), dict(bad_layer=True), dict(repeat=True)])
+def test_hybrid_simulation_rejects_broken_lists(kw):
+    t, n, off, idx = hybrid_lists(**kw)
+    with pytest.raises(AssertionError):
+        oracle.simulate(t, n, NCTR, 2, 3, seed=3, trials=20, list_off=off, list_idx=idx,
+                        att_first=ATT_FIRST, att_count=4)
