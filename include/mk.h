@@ -90,7 +90,8 @@ typedef struct mk_config {
   int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   float rms_eps, rope_theta;
   int32_t tie_embeddings;  /* 1: the LM head is the embedding matrix */
-  int32_t batch;           /* sequences per step, 1..16 */
+  int32_t batch;           /* sequences per step: 1..16, or 32 or 48 (larger-batch mode:
+                              tensor cores, 16 KB pages unless page_bytes says otherwise) */
   int32_t max_ctx;         /* KV capacity per sequence (positions), multiple of 16 */
   int32_t sched_mode;      /* MK_SCHED_DYNAMIC, MK_SCHED_STATIC or MK_SCHED_HYBRID */
   uint32_t flags;          /* MK_FLAG_* */
@@ -206,7 +207,7 @@ MK_API const char *mk_error_string(int code);
    device and upload the tables and the RoPE table.  Errors: MK_ERR_ARG (NULL),
    MK_ERR_CONFIG (shape not plannable: hidden/ffn not multiples of 256,
    n_q_heads not a multiple of n_kv_heads or more than 8 q heads per group,
-   head_dim not 64 or 128, batch outside 1..16, max_ctx not a positive
+   head_dim not 64 or 128, batch not in 1..16 or 32 or 48, max_ctx not a positive
    multiple of 16, shared memory too small), MK_ERR_DEVICE (not an sm_103
    device), MK_ERR_NOMEM.  On success *out owns everything; free it with
    mk_destroy. */

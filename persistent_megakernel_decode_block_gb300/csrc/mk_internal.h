@@ -13,7 +13,7 @@ namespace mk {
 constexpr int kComputeWarps = 14;  // 16 warps per block: 4 per SM sub-partition, 128 registers each
 constexpr int kThreads = 32 * (2 + kComputeWarps);
 constexpr int kFifo = 8;        // instructions a block may hold ahead of compute
-constexpr int kMaxBatch = 16;
+constexpr int kMaxBatch = 48;   // 1..16, or 32 / 48 (tensor-core readback in blocks of 16)
 constexpr int kMaxQpg = 8;      // q heads per KV group
 constexpr int kMaxItems = 256;  // work items (row x slice) per GEMV instruction
 constexpr int kMaxItemsB = 256; // work items x batch per GEMV instruction
@@ -73,7 +73,8 @@ struct KParams {
   int32_t nchunk, attn_chunk, att_lmax;
   int32_t tc, tc_nb;  // tensor-core projections (batch > 1); MMA N = 2 x batch rounded up to 16
   int32_t stream;     // batch 1: compute warps stream their own weights (per-warp rings)
-  int32_t att_grp;    // attention warps serve all query heads of the group (attn_chunk_grp)
+  int32_t att_grp;
+  uint32_t tmem_cols;  // tensor-core plans: tensor-memory columns of the accumulator    // attention warps serve all query heads of the group (attn_chunk_grp)
   uint32_t wnb;       // stream plans: slots (512 B) in each compute warp's ring
   float *gpart;       // partial sums of split projections [block][slice][MR][B]
   float eps, attn_scale;

@@ -769,34 +769,40 @@ __device__ __noinline__ bool gemv_tc(const KParams &P, const Smem &S, const mk_i
     if (!warp_wait(P, S, S.tbar, tc_uses & 1u, kWhereCompute | meta.idx)) return false;
     if (32 * qd < MR) {
       tc_fence_after();
-      float v[32];
-      float(&v0)[16] = *reinterpret_cast<float(*)[16]>(v);
-      float(&v1)[16] = *reinterpret_cast<float(*)[16]>(v + 16);
       const uint32_t ta = taddr + ((uint32_t)(32 * qd) << 16);
-      tc_ld16(ta, v0);
-      if (NB > 16) tc_ld16(ta + 16, v1);
       const int r = 32 * qd + lane;
-      if (direct && in.op == MK_OP_LMHEAD) {
-        if (r < (int)in.nrows)
+      const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
+      float *gdst = P.gpart + (((size_t)rb * in.nchunk + in.chunk) * MR + r) * B;
+      // one output (row r, sequence b) = value column b + remainder column B + b
+      auto emit = [&](int b, float x) {
+        if (direct && in.op == MK_OP_LMHEAD) {
+          if (r < (int)in.nrows) P.logits[(size_t)b * P.V + in.row0 + r] = x;
+        } else if (direct) {  // gate/up: lane 2j holds gate j, lane 2j + 1 up j
+          const int jg = r / 2;
+          const float up = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+          if (!(lane & 1) && jg < (int)in.nrows)
+            P.h[(size_t)b * P.F + in.row0 + jg] = x / (1.f + __expf(-x)) * up;
+        } else {
+          gdst[b] = x;
+        }
+      };
+      if (B <= 16) {  // values and remainders within the first 32 columns
+        float v[32];
+        float(&v0)[16] = *reinterpret_cast<float(*)[16]>(v);
+        float(&v1)[16] = *reinterpret_cast<float(*)[16]>(v + 16);
+        tc_ld16(ta, v0);
+        if (NB > 16) tc_ld16(ta + 16, v1);
 #pragma unroll
-          for (int b = 0; b < kMaxBatch; ++b)
-            if (b < B) P.logits[(size_t)b * P.V + in.row0 + r] = v[b] + v[B + b];
-      } else if (direct) {  // gate/up: lane 2j holds gate j, lane 2j + 1 up j
-        const int j = r / 2;
+        for (int b = 0; b < 16; ++b)
+          if (b < B) emit(b, v[b] + v[B + b]);
+      } else {  // B a multiple of 16: sixteen sequences' values and remainders at a time
+        for (int b0 = 0; b0 < B; b0 += 16) {
+          float va[16], vr[16];
+          tc_ld16(ta + (uint32_t)b0, va);
+          tc_ld16(ta + (uint32_t)(B + b0), vr);
 #pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b)
-          if (b < B) {
-            const float x = v[b] + v[B + b];
-            const float up = __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-            if (!(lane & 1) && j < (int)in.nrows)
-              P.h[(size_t)b * P.F + in.row0 + j] = x / (1.f + __expf(-x)) * up;
-          }
-      } else {
-        const int rb = (int)in.row0 / (in.op == MK_OP_GATEUP ? MR / 2 : MR);
-        float *dst = P.gpart + (((size_t)rb * in.nchunk + in.chunk) * MR + r) * B;
-#pragma unroll
-        for (int b = 0; b < kMaxBatch; ++b)
-          if (b < B) dst[b] = v[b] + v[B + b];
+          for (int b = 0; b < 16; ++b) emit(b0 + b, va[b] + vr[b]);
+        }
       }
     }
   }
@@ -1547,11 +1553,12 @@ DEVI void megakernel_body(const KParams &P) {
     return;
   }
   if (TC) {
-    // tensor memory for the projections' accumulator (at most 32 fp32
+    // tensor memory for the projections' accumulator (tmem_cols fp32
+    // columns, a power of two >= 32 covering the 2B value and remainder
     // columns), and a zeroed B-operand buffer (rows past 2B stay zero)
     if (warp == 2) {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(
-                       saddr((const void *)(S.misc + 3)))
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       saddr((const void *)(S.misc + 3))), "r"(P.tmem_cols)
                    : "memory");
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -1593,7 +1600,8 @@ DEVI void megakernel_body(const KParams &P) {
     __syncthreads();
     tc_fence_after();
     if (warp == 2)
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 32;" ::"r"((uint32_t)S.misc[3])
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"((uint32_t)S.misc[3]),
+                   "r"(P.tmem_cols)
                    : "memory");
   }
   // a block only bails after a latched error; never let it end silently

@@ -51,14 +51,17 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   if (c.head_dim != 64 && c.head_dim != 128) REJECT("head_dim must be 64 or 128");
   if ((c.n_q_heads * c.head_dim) % 256) REJECT("n_q_heads*head_dim must be a multiple of 256");
   if (c.vocab < 1) REJECT("vocab must be positive");
-  if (c.batch < 1 || c.batch > kMaxBatch) REJECT("batch must be in 1..16");
+  if (c.batch < 1 || c.batch > kMaxBatch || (c.batch > 16 && c.batch % 16))
+    REJECT("batch must be in 1..16, or 32 or 48");
   if (c.max_ctx < 16 || c.max_ctx % 16) REJECT("max_ctx must be a positive multiple of 16");
   if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0f)) REJECT("rms_eps >= 0 and rope_theta > 0 required");
   if (c.sched_mode != MK_SCHED_DYNAMIC && c.sched_mode != MK_SCHED_STATIC &&
       c.sched_mode != MK_SCHED_HYBRID)
     REJECT("bad sched_mode");
   if (num_sms < 1 || num_sms > 1024) REJECT("number of SMs out of range");
-  const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : 32768u;
+  // larger batches (32, 48) default to 16 KB pages: a page's B operand is then
+  // batch x 64 columns, one (sequence, 8 columns) unit per staging thread
+  const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : c.batch > 16 ? 16384u : 32768u;
   if (page < 4096 || page > 65536 || page % 1024) REJECT("page_bytes must be a multiple of 1024 in 4096..65536");
 
   P = HostPlan();
@@ -131,6 +134,9 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.stream = B == 1 && (c.flags & MK_FLAG_STREAM_B1);
   if (P.tc) {
     P.tc_nb = 16 * cdiv(2 * (uint32_t)B, 16);
+    // accumulator columns in tensor memory: a power of two >= 32
+    P.tmem_cols = 32;
+    while (P.tmem_cols < P.tc_nb) P.tmem_cols *= 2;
     const uint32_t rows_of[8] = {0, (uint32_t)(nkv * GR), 0, (uint32_t)H, (uint32_t)(2 * F),
                                  (uint32_t)H, (uint32_t)V, 0};
     for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {

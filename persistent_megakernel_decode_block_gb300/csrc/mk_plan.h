@@ -32,6 +32,7 @@ struct HostPlan {
   uint32_t attn_chunk = 0, nchunk = 0, att_lmax = 0;
   bool tc = false;              // batch > 1: projections on tcgen05, split along K
   bool stream = false;          // batch 1: every compute warp streams its own weights
+  uint32_t tmem_cols = 32;      // tensor-core plans: tensor-memory columns allocated
   bool att_grp = false;         // tensor-core plans, d = 64, <= 4 heads per group: every
                                 // attention warp serves all heads of the group
   uint32_t wnb = 0;             // stream plans: ring slots (512 B) per compute warp

@@ -204,6 +204,7 @@ static int setup_device(mk_plan_s *p) {
   P.tc_nb = (int32_t)H.tc_nb;
   P.stream = H.stream ? 1 : 0;
   P.att_grp = H.att_grp ? 1 : 0;
+  P.tmem_cols = H.tmem_cols;
   P.wnb = H.wnb;
   P.off_wring = H.off_wring;
   P.gpart = p->d_gpart;

@@ -43,6 +43,10 @@ WORKLOADS = {
     "llama8b_ctx2048": dict(model=LLAMA8B, batch=1, ctx=2048, steps=64),
     # small batched parity case (the tensor-core projections of batch > 1)
     "tiny_b4_ragged": dict(model=TINY, batch=4, ctx=(16, 64), steps=8),
+    # larger-batch mode (batch 32: tensor cores, 16 KB pages, accumulator
+    # read back sixteen sequences at a time)
+    "tiny_b32_ragged": dict(model=TINY, batch=32, ctx=(16, 64), steps=8),
+    "llama1b_b32_ragged": dict(model=LLAMA1B, batch=32, ctx=(128, 4096), steps=64),
 }
 ORDER = ["tiny", "llama1b_ctx1024", "llama1b_ctx8192", "llama1b_b8_ragged", "llama8b_ctx2048"]
 

@@ -87,6 +87,23 @@ def test_tiny_batched_tensor_core_path(sched):
         s.close()
 
 
+@pytest.mark.parametrize("name, steps, sched", [
+    ("tiny_b32_ragged", 8, mk.MK_SCHED_DYNAMIC), ("tiny_b32_ragged", 8, mk.MK_SCHED_STATIC),
+    ("tiny_b32_ragged", 8, mk.MK_SCHED_HYBRID), ("llama1b_b32_ragged", 1, mk.MK_SCHED_STATIC)])
+def test_larger_batch_mode(name, steps, sched):
+    """Batch 32: tensor cores with 16 KB pages, the accumulator read back
+    sixteen sequences at a time; teacher-forced against the oracle."""
+    s = Setup(name, sched=sched, steps=steps)
+    try:
+        assert s.info["kernel"] == 1 and s.info["page_bytes"] == 16384
+        worst = teacher_forced(s, steps)
+        print("%s: %d steps, worst max|d|=%.3g relL2=%.3g" % (name, steps, *worst))
+        check_counters(s, steps)
+        kv_matches_oracle(s)
+    finally:
+        s.close()
+
+
 @pytest.mark.parametrize("sched", [mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
 def test_static_and_hybrid_schedules_full_size(sched):
     s = Setup("llama1b_ctx1024", sched=sched)
