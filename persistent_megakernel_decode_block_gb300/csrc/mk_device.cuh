@@ -181,6 +181,8 @@ struct Smem {
   float *res, *opart, *ml, *sc, *rope, *normr, *rbuf, *xs;
   uint32_t *sat;
   int32_t *pos, *tok;
+  uint64_t *dmask;     // attention re-deal: per chunk, the sequences it has work for
+  uint32_t *dpre;      // and the prefix count of (chunk, sequence) pairs with work
   volatile int *misc;  // [0] bail, [1] bad input
 };
 
@@ -215,6 +217,8 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.rope = reinterpret_cast<float *>(base + P.off_rope);
   S.normr = reinterpret_cast<float *>(base + P.off_normr);
   S.misc = reinterpret_cast<volatile int *>(base + P.off_misc);
+  S.dmask = reinterpret_cast<uint64_t *>(base + P.off_deal);
+  S.dpre = reinterpret_cast<uint32_t *>(S.dmask + kMaxDealChunks);
   S.rbuf = reinterpret_cast<float *>(base + P.off_rbuf);
   S.xs = reinterpret_cast<float *>(base + P.off_xs);
   S.wring = base + P.off_wring;

@@ -22,6 +22,7 @@ constexpr int kMaxChunks = 4;   // 256-column chunks per item: the input slice a
 constexpr int kTcBufs = 4;     // ring slots of the tensor-core B operand (one page's columns each)
 constexpr int kCtrStride = 32;  // u32 words between counters (128 B apart)
 constexpr int kMaxRing = 32;
+constexpr int kMaxDealChunks = 256;  // attention chunks per (sequence, group) the re-deal tabulates
 // stream plans: each compute warp's ring of 512-byte slots is filled by
 // per-lane async copies in commit groups of kSG slots
 constexpr int kSG = 4;
@@ -87,7 +88,7 @@ struct KParams {
   // dynamic shared-memory layout (byte offsets)
   uint32_t ring_pages, page_bytes;
   uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,
-      off_rope, off_normr, off_misc, off_rbuf, off_xs, off_wring, smem_total;
+      off_rope, off_normr, off_misc, off_rbuf, off_xs, off_wring, off_deal, smem_total;
 };
 
 // per FIFO slot metadata written by the loader

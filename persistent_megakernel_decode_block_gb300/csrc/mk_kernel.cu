@@ -112,9 +112,44 @@ DEVI void load_record(const KParams &P, uint32_t idx, uint4 (&r)[4]) {
 // SMs like the slots.  Rewrites the FIFO copy of the record (chunk, sequence,
 // group and their two counters, affine in sequence and group) and returns the
 // index of the instruction it now is.
+// n-th (0-based) set bit of a 64-bit mask that has more than n set bits
+DEVI int nth_set_bit(uint64_t m, int n) {
+  const uint32_t lo = (uint32_t)m, hi = (uint32_t)(m >> 32);
+  const int nlo = __popc(lo);
+  return n < nlo ? (int)__fns(lo, 0, n + 1) : 32 + (int)__fns(hi, 0, n - nlo + 1);
+}
+
 DEVI uint32_t balance_attn(const KParams &P, const Smem &S, mk_instr &in, uint32_t idx) {
   const int B = P.B, G = P.nkv, C = (int)in.nchunk, ch = P.attn_chunk;
   const int j = ((int)in.chunk * B + in.b) * G + in.g;
+  if (C <= kMaxDealChunks) {
+    // from the launch's tables: binary search of the chunk, the rank's
+    // sequence as the n-th set bit of the chunk's mask (or of its complement)
+    const int nreal = (int)S.dpre[C] * G;
+    const bool want_real = j < nreal;
+    const int r = want_real ? j : j - nreal;
+    const int q = r / G, g = r % G;  // rank of the (chunk, sequence) pair, group
+    auto before = [&](int c) {        // pairs of the wanted kind in chunks < c
+      return want_real ? (int)S.dpre[c] : c * B - (int)S.dpre[c];
+    };
+    int lo = 0, hi = C - 1;  // last chunk c with before(c) <= q
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) / 2;
+      if (before(mid) <= q) lo = mid;
+      else hi = mid - 1;
+    }
+    const int c = lo;
+    const uint64_t all = B == 64 ? ~0ull : (1ull << B) - 1ull;
+    const uint64_t m = want_real ? S.dmask[c] : (~S.dmask[c] & all);
+    const int b = nth_set_bit(m, q - before(c));
+    const int jn = (c * B + b) * G + g;
+    in.sig_ctr = in.sig_ctr + (uint32_t)((b - (int)in.b) * G + (g - (int)in.g));
+    in.wait_ctr = in.wait_ctr + (uint32_t)(g - (int)in.g);
+    in.chunk = (uint32_t)c;
+    in.b = (uint16_t)b;
+    in.g = (uint16_t)g;
+    return idx - (uint32_t)j + (uint32_t)jn;
+  }
   // sequences whose position reaches chunk c: those with pos >= c * ch
   auto live = [&](int c) {
     int n = 0;
@@ -1537,6 +1572,26 @@ DEVI void megakernel_body(const KParams &P) {
     if (t < 0 || t >= P.V || p < 0 || p >= P.max_ctx) S.misc[1] = 1;
   }
   __syncthreads();
+  if (TC && P.nchunk <= kMaxDealChunks) {
+    // the attention re-deal's tables for this launch's positions (the same
+    // for every layer): chunk c has work for sequence b when p_b >= c * chunk
+    for (int c = tid; c < P.nchunk; c += kThreads) {
+      uint64_t m = 0;
+      for (int b = 0; b < P.B; ++b)
+        if (S.pos[b] >= c * P.attn_chunk) m |= 1ull << b;
+      S.dmask[c] = m;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t acc = 0;
+      for (int c = 0; c < P.nchunk; ++c) {
+        S.dpre[c] = acc;
+        acc += (uint32_t)__popcll(S.dmask[c]);
+      }
+      S.dpre[P.nchunk] = acc;
+    }
+    __syncthreads();
+  }
   const bool bad = S.misc[1] != 0;
   if (!bad) {
     const int half = P.d / 2;

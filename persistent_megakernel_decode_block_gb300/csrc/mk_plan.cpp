@@ -252,6 +252,10 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   uint32_t rel_rope = take(B * d * 4, 16);
   uint32_t rel_normr = take(2 * kMaxBatch * 4, 16);  // double-buffered per input change
   uint32_t rel_misc = take(kMiscDescOffset + kMiscDescBytes, 16);  // flags, then the pointer table
+  // the attention re-deal's per-launch tables: per chunk, the mask of the
+  // sequences it has work for, and the prefix count of chunk-sequence pairs
+  // with work
+  uint32_t rel_deal = take(P.tc ? kMaxDealChunks * 8 + (kMaxDealChunks + 1) * 4 : 0, 16);
   uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
   // staged GEMV input (normalised x, or the attention output) and attention scores
   uint32_t xs_floats = std::max<uint32_t>(H, QD);
@@ -302,6 +306,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.off_rope = ring + rel_rope;
   P.off_normr = ring + rel_normr;
   P.off_misc = ring + rel_misc;
+  P.off_deal = ring + rel_deal;
   P.off_rbuf = ring + rel_rbuf;
   P.off_xs = ring + rel_xs;
   P.off_bars = ring + rel_bars;

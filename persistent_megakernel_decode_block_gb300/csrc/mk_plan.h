@@ -42,7 +42,8 @@ struct HostPlan {
   // shared-memory layout
   uint32_t ring_pages = 0, page_bytes = 0, res_floats = 0;
   uint32_t off_bars = 0, off_fifo = 0, off_meta = 0, off_res = 0, off_att = 0, off_sat = 0,
-           off_pos = 0, off_rope = 0, off_normr = 0, off_misc = 0, off_rbuf = 0, off_xs = 0, off_wring = 0, smem_total = 0;
+           off_pos = 0, off_rope = 0, off_normr = 0, off_misc = 0, off_rbuf = 0, off_xs = 0, off_wring = 0, off_deal = 0,
+           smem_total = 0;
   uint32_t fault_instr = 0xFFFFFFFFu;
 };
 

@@ -241,6 +241,7 @@ static int setup_device(mk_plan_s *p) {
   P.off_rope = H.off_rope;
   P.off_normr = H.off_normr;
   P.off_misc = H.off_misc;
+  P.off_deal = H.off_deal;
   P.off_rbuf = H.off_rbuf;
   P.off_xs = H.off_xs;
   P.smem_total = H.smem_total;
