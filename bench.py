@@ -447,7 +447,8 @@ def run_mine(a):
     torch.cuda.empty_cache()
     if rank == 0 and not a.no_workloads and name == DEFAULT and not a.layers and not a.trace:
         extra["workloads"] = {o: time_workload(mk, torch, dev, o, a) for o in
-                              ("llama1b_ctx8192", "llama1b_b8_ragged", "llama8b_ctx2048")}
+                              ("llama1b_ctx8192", "llama1b_b8_ragged", "llama1b_b32_ragged",
+                               "llama8b_ctx2048")}
     if rank != 0:
         return
     line = {

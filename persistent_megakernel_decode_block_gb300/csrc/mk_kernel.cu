@@ -1182,7 +1182,9 @@ __device__ __noinline__ bool attn_chunk(const KParams &P, const Smem &S, const m
 // single-buffered: the per-head merge reads them before the barrier that
 // precedes the arrival, which every warp passes before it can reach the next
 // chunk.
-template <int QPG>
+// MP: the chunk may span several key (and value) pages (chunks longer than
+// a page); otherwise every row is in the chunk's one key and one value page.
+template <int QPG, bool MP>
 __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, const mk_instr &in,
                                             const SlotMeta &meta, int cw, int lane,
                                             uint32_t &att_uses, uint32_t epoch) {
@@ -1233,11 +1235,41 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
     }
   }
   if (stamp) mw.t_input = gtimer();
-  const bool paged = n_old > 0;  // one key page and one value page
-  const uint8_t *__restrict__ kpage = S.ring + (size_t)(meta.seq0 % E) * P.page_bytes;
-  const uint8_t *__restrict__ vpage = S.ring + (size_t)((meta.seq0 + 1) % E) * P.page_bytes;
-  if (paged && !warp_wait(P, S, &S.full[meta.seq0 % E], (meta.seq0 / E) & 1u, kWhereCompute | meta.idx))
-    return false;
+  // keys of the cached rows arrive as npk ring pages of rpp rows each (a power
+  // of two), then their values as npk more; a warp's rows span at most two
+  // pages, whose addresses it works out once
+  const int rs = __ffs((int)P.page_bytes / (D * 2)) - 1, rpp = 1 << rs;
+  const int npk = (n_old + rpp - 1) >> rs;
+  const bool paged = n_old > 0;
+  const int pg0 = j0 >> rs;
+  const uint8_t *base[2][2];
+#pragma unroll
+  for (int side = 0; side < 2; ++side)
+#pragma unroll
+    for (int k = 0; k < (MP ? 2 : 1); ++k) {
+      const uint32_t seq = meta.seq0 + (uint32_t)(MP ? side * npk + pg0 + k : side);
+      base[side][k] = S.ring + (size_t)(seq % E) * P.page_bytes;
+    }
+  auto row_ptr = [&](int side, int j) {  // side 0 keys, 1 values; j0 <= j < n_old
+    if (!MP) return base[side][0] + (size_t)j * D * 2;  // pg0 = 0, one page per side
+    return base[side][(j >> rs) - pg0] + (size_t)(j & (rpp - 1)) * D * 2;
+  };
+  auto wait_rows = [&](int side) -> bool {  // the pages holding rows j0 .. j1 - 1
+    if (!MP) {
+      if (!paged) return true;
+      const uint32_t seq = meta.seq0 + (uint32_t)side;
+      return warp_wait(P, S, &S.full[seq % E], (seq / E) & 1u, kWhereCompute | meta.idx);
+    }
+    const int jl = min(j1, n_old);
+    if (j0 >= jl) return true;
+    for (int pg = j0 / rpp; pg <= (jl - 1) / rpp; ++pg) {
+      const uint32_t seq = meta.seq0 + (uint32_t)(side * npk + pg);
+      if (!warp_wait(P, S, &S.full[seq % E], (seq / E) & 1u, kWhereCompute | meta.idx))
+        return false;
+    }
+    return true;
+  };
+  if (!wait_rows(0)) return false;
 
   // 1. scores of rows j0..j1 for every head: a block of LPP steps covers 32
   //    rows; per head one transposing butterfly over the LPP lanes of a row
@@ -1247,7 +1279,7 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
   auto score8 = [&](int j, float (&out)[QPG]) {
     float k8[8];
     if (j < n_old) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(kpage + (size_t)j * D * 2 + part * 16);
+      const uint4 w = *reinterpret_cast<const uint4 *>(row_ptr(0, j) + part * 16);
       k8[0] = bf_lo(w.x); k8[1] = bf_hi(w.x); k8[2] = bf_lo(w.y); k8[3] = bf_hi(w.y);
       k8[4] = bf_lo(w.z); k8[5] = bf_hi(w.z); k8[6] = bf_lo(w.w); k8[7] = bf_hi(w.w);
     } else {
@@ -1317,9 +1349,7 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
 
   // 3. o[h] = sum_j p_j[h] v_j over this warp's rows; lanes own DPL dims,
   //    even and odd rows in separate accumulators
-  if (paged && !warp_wait(P, S, &S.full[(meta.seq0 + 1) % E], ((meta.seq0 + 1) / E) & 1u,
-                          kWhereCompute | meta.idx))
-    return false;
+  if (!wait_rows(1)) return false;
   if (stamp) mw.t_pagel = gtimer();
   float o[2][QPG][DPL];
 #pragma unroll
@@ -1328,7 +1358,6 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
     for (int h = 0; h < QPG; ++h)
 #pragma unroll
       for (int k = 0; k < DPL; ++k) o[e][h][k] = 0.f;
-  const uint8_t *__restrict__ vrow = vpage + lane * DPL * 2;
   for (int j = j0; j < j1; j += 2) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -1336,7 +1365,7 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
       if (jj < j1) {
         float vv[DPL];
         if (jj < n_old) {
-          const uint32_t w = *reinterpret_cast<const uint32_t *>(vrow + (size_t)jj * D * 2);
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(row_ptr(1, jj) + lane * DPL * 2);
           vv[0] = bf_lo(w);
           vv[1] = bf_hi(w);
         } else {
@@ -1372,8 +1401,12 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
   }
   if (!compute_sync(P, S, S.attbar, att_uses, lane)) return false;
   if (paged && cw == 0 && lane == 0) {  // every warp is past the pages
-    mbar_arrive(&S.empty[meta.seq0 % E]);
-    mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
+    if (MP) {
+      for (int pg = 0; pg < 2 * npk; ++pg) mbar_arrive(&S.empty[(meta.seq0 + (uint32_t)pg) % E]);
+    } else {
+      mbar_arrive(&S.empty[meta.seq0 % E]);
+      mbar_arrive(&S.empty[(meta.seq0 + 1) % E]);
+    }
   }
 
   // 5. warp hh < QPG merges the partials of head hh into the chunk partial
@@ -1414,10 +1447,17 @@ DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
                         uint32_t epoch) {
   if constexpr (TC) {
     if (P.att_grp) {
+      if (P.attn_chunk > (int)P.page_bytes / 128) {
+        switch (P.qpg) {
+          case 1: return attn_chunk_grp<1, true>(P, S, in, meta, cw, lane, att_uses, epoch);
+          case 2: return attn_chunk_grp<2, true>(P, S, in, meta, cw, lane, att_uses, epoch);
+          default: return attn_chunk_grp<4, true>(P, S, in, meta, cw, lane, att_uses, epoch);
+        }
+      }
       switch (P.qpg) {
-        case 1: return attn_chunk_grp<1>(P, S, in, meta, cw, lane, att_uses, epoch);
-        case 2: return attn_chunk_grp<2>(P, S, in, meta, cw, lane, att_uses, epoch);
-        default: return attn_chunk_grp<4>(P, S, in, meta, cw, lane, att_uses, epoch);
+        case 1: return attn_chunk_grp<1, false>(P, S, in, meta, cw, lane, att_uses, epoch);
+        case 2: return attn_chunk_grp<2, false>(P, S, in, meta, cw, lane, att_uses, epoch);
+        default: return attn_chunk_grp<4, false>(P, S, in, meta, cw, lane, att_uses, epoch);
       }
     }
   }

@@ -206,11 +206,16 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // (checked once the ring size is known); start from 128 positions at
   // d = 64 and 64 at d = 128.
   const uint32_t rpp = page / (2 * (uint32_t)d);  // key (or value) rows per page
-  const uint32_t ch_cap = P.stream ? (d == 64 ? 128u : 64u) : rpp;
+  // Tensor-core plans with d = 64 and at most four heads per group run the
+  // grouped chunk, whose keys and values may span several pages: chunks of
+  // up to 256 positions there even with 16 KB pages.
+  P.att_grp = P.tc && d == 64 && qpg <= 4 && (page & (page - 1)) == 0;
+  const uint32_t ch_cap = P.stream ? (d == 64 ? 128u : 64u) : P.att_grp ? std::max(rpp, 256u) : rpp;
   uint32_t ch = c.attn_chunk > 0 ? (uint32_t)c.attn_chunk : ch_cap;
   if (c.attn_chunk <= 0)
     while (ch > 64 && (uint64_t)B * nkv * cdiv(c.max_ctx, ch) < num_sms / 2) ch /= 2;
-  if (ch % 16 || ch < 16 || (!P.stream && ch > rpp) || ch > 1024)
+  if (ch % 16 || ch < 16 || (!P.stream && !P.att_grp && ch > rpp) || ch > 1024 ||
+      (P.att_grp && ch > 32u * kComputeWarps))
     REJECT("attn_chunk must be a multiple of 16 and at most one page of keys");
   P.attn_chunk = ch;
   P.nchunk = cdiv(c.max_ctx, ch);
@@ -219,7 +224,6 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // most four heads per group split a chunk's positions over all compute
   // warps instead, each warp scoring its rows for every head of the group
   // (one read of each key and value row per warp): scores [row][head].
-  P.att_grp = P.tc && d == 64 && qpg <= 4;
   P.att_lmax = P.att_grp
                    ? (uint32_t)align_up((uint64_t)cdiv(ch, (uint32_t)kComputeWarps) * qpg, 4)
                    : (uint32_t)align_up(cdiv(ch, (uint32_t)(kComputeWarps / qpg)), 4);
@@ -293,6 +297,8 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   } else {
     uint32_t E = std::min<uint32_t>(kMaxRing, avail / page);
     if (E < 2) REJECT("shared memory too small for a two-page ring");
+    if (P.att_grp && 2 * cdiv(P.attn_chunk, rpp) > E)
+      REJECT("ring too small for an attention chunk's key and value pages");
     P.ring_pages = E;
     ring = (uint32_t)align_up(E * page, 1024);
   }

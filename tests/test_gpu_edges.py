@@ -95,19 +95,26 @@ def test_batch1_edges(case, stream):
 # chunks): sequence 0 from position 0, 1 across the chunk boundary at 64, 2 up
 # to max_ctx - 1, 3 inside chunk 0.
 BATCHED = {
-    "tiny_b4": ("tiny_b4_ragged", [0, 60, 120, 31], 128, 8, 64),
+    "tiny_b4": ("tiny_b4_ragged", [0, 60, 120, 31], 128, 8, 64, {}),
     # Llama-1B batch 8, max_ctx 4096, 256-position chunks (one key page):
     # sequences from 0, across 256, 1024, 2048 and 3072, and up to 4095
     "llama1b_b8": ("llama1b_b8_ragged", [0, 255, 254, 1022, 2047, 4093, 129, 3071], 4096, 3,
-                   256),
+                   256, {}),
+    # batch 32 (16 KB pages: 128 keys per page) with 256-position chunks, so
+    # a chunk's keys and values span two pages each: sequences at 0, across
+    # the page boundary inside a chunk (128), across chunk boundaries (256),
+    # and up to max_ctx - 1
+    "tiny_b32_2pages": ("tiny_b32_ragged",
+                        [0, 126, 127, 250, 255, 380, 508, 60] * 4, 512, 4, 256,
+                        {"attn_chunk": 256}),
 }
 
 
 @pytest.mark.parametrize("case", sorted(BATCHED))
 @pytest.mark.parametrize("sched", [mk.MK_SCHED_DYNAMIC, mk.MK_SCHED_STATIC, mk.MK_SCHED_HYBRID])
 def test_batched_edges(case, sched):
-    name, ctx, mctx, steps, chunk = BATCHED[case]
-    s = Setup(name, ctx=ctx, mctx=mctx, sched=sched)
+    name, ctx, mctx, steps, chunk, kw = BATCHED[case]
+    s = Setup(name, ctx=ctx, mctx=mctx, sched=sched, **kw)
     try:
         assert s.info["kernel"] == 1
         worst = run_window(s, steps, chunk)
@@ -120,9 +127,9 @@ def test_batched_edges(case, sched):
 def test_redealt_schedule_matches_the_oracle(case):
     """Static lists, batch > 1: every instruction ran on the block whose list
     slot the oracle's re-deal gives it for the step's positions, once."""
-    name, ctx, mctx, _, _ = BATCHED[case]
+    name, ctx, mctx, _, _, kw = BATCHED[case]
     s = Setup(name, ctx=ctx, mctx=mctx, sched=mk.MK_SCHED_STATIC, flags=mk.MK_FLAG_TRACE,
-              with_oracle=False)
+              with_oracle=False, **kw)
     try:
         _, raw, _ = mk.mk_plan_tables(s.plan)
         off, idx = mk.mk_plan_lists(s.plan)
