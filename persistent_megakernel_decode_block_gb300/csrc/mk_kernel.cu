@@ -1437,8 +1437,11 @@ __device__ __noinline__ bool attn_chunk_grp(const KParams &P, const Smem &S, con
     }
   }
 
-  // 6. arrival, and the group merge by its last chunk
-  return attn_arrive_merge<D, QPG>(P, S, in, cw, lane, att_uses, epoch, b, g, pos);
+  // 6. the chunk partial is in global memory once every warp is past this
+  //    barrier (which also frees the per-warp partials for the next chunk);
+  //    the storer takes the arrival and, for the group's last chunk, merges
+  (void)epoch;
+  return compute_sync(P, S, S.attbar, att_uses, lane);
 }
 
 template <bool TC>
@@ -1547,6 +1550,99 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
 }
 
 
+// Tensor-core plans with grouped attention: the storer warp takes a chunk's
+// arrival off the compute warps (which go on to their next instruction once
+// the chunk partial is written), and merges the group when its chunk is the
+// last to arrive.  The compute warps' partial writes are ordered before the
+// arrival through the slot's done barrier (the compute warps' release at CTA
+// scope, this warp's acquire) and the arrival's own gpu-scope release.  The
+// merge by one warp: lane c holds the maxima and denominators of chunk
+// c0 + c for every head; each lane owns OPL consecutive outputs of one head
+// and accumulates them over the chunks, CB chunks' loads in flight.
+template <int QPG>
+__device__ __noinline__ void storer_attn_grp(const KParams &P, const Smem &S, const mk_instr &in,
+                                             int lane, uint32_t epoch) {
+  constexpr int D = 64, PS = 2 * QPG + QPG * D, OPL = QPG * D / 32, CB = 4;
+  const int b = in.b, g = in.g, pos = S.pos[b];
+  int p0, p1;
+  attn_range(P, pos, in.chunk, p0, p1);
+  if (p1 - p0 <= 0) return;  // past p_b: no arrival (the last real chunk adds it)
+  const int nch = min((int)in.nchunk, (pos + P.attn_chunk) / P.attn_chunk);
+  int last = 0;
+  if (lane == 0) {
+    uint32_t *ctr = P.ctr + (size_t)in.sig_ctr * kCtrStride;
+    const uint32_t old = atom_add_acq_rel(ctr, 1u);
+    last = old == epoch * in.nchunk + (uint32_t)nch - 1u ? 1 : 0;
+    if (last && (uint32_t)nch < in.nchunk) red_add(ctr, in.nchunk - (uint32_t)nch);
+  }
+  if (!__shfl_sync(0xFFFFFFFFu, last, 0)) return;
+  const float *pb = P.part + ((size_t)b * P.nkv + g) * in.nchunk * PS;
+  const int o0 = lane * OPL, hl = o0 / D;
+  float M[QPG], den[QPG], num[OPL];
+#pragma unroll
+  for (int h = 0; h < QPG; ++h) {
+    M[h] = -INFINITY;
+    den[h] = 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < OPL; ++k) num[k] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const bool valid = c < nch;
+    float w[QPG], a[QPG];
+#pragma unroll
+    for (int h = 0; h < QPG; ++h) {
+      const float mh = valid ? __ldcg(pb + (size_t)c * PS + h) : -INFINITY;
+      const float lh = valid ? __ldcg(pb + (size_t)c * PS + QPG + h) : 0.f;
+      const float Mn = fmaxf(M[h], warp_max(mh));
+      a[h] = M[h] == -INFINITY ? 0.f : __expf(M[h] - Mn);
+      w[h] = mh == -INFINITY ? 0.f : __expf(mh - Mn);
+      den[h] = den[h] * a[h] + warp_sum(w[h] * lh);
+      M[h] = Mn;
+    }
+    float ah = a[0];
+#pragma unroll
+    for (int h = 1; h < QPG; ++h) ah = hl == h ? a[h] : ah;
+#pragma unroll
+    for (int k = 0; k < OPL; ++k) num[k] *= ah;
+    const int nb = min(32, nch - c0);
+    for (int cb = 0; cb < nb; cb += CB) {
+      float oc[CB][OPL];
+#pragma unroll
+      for (int u = 0; u < CB; ++u)
+        if (cb + u < nb) {
+          const float *src = pb + (size_t)(c0 + cb + u) * PS + 2 * QPG + o0;
+#pragma unroll
+          for (int k = 0; k < OPL; k += 4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + k));
+            oc[u][k] = v.x; oc[u][k + 1] = v.y; oc[u][k + 2] = v.z; oc[u][k + 3] = v.w;
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < CB; ++u)
+        if (cb + u < nb) {
+          float wu = 0.f;
+#pragma unroll
+          for (int h = 0; h < QPG; ++h) {
+            const float wh = __shfl_sync(0xFFFFFFFFu, w[h], cb + u);
+            wu = hl == h ? wh : wu;
+          }
+#pragma unroll
+          for (int k = 0; k < OPL; ++k) num[k] = fmaf(wu, oc[u][k], num[k]);
+        }
+    }
+  }
+  float dh = den[0];
+#pragma unroll
+  for (int h = 1; h < QPG; ++h) dh = hl == h ? den[h] : dh;
+  float *dst = P.attn + (size_t)b * P.nq * D + (size_t)g * QPG * D + o0;
+#pragma unroll
+  for (int k = 0; k < OPL; ++k) dst[k] = num[k] / dh;
+  __syncwarp();
+  if (lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
+}
+
+template <bool TC>
 DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
   for (uint32_t fs = 0;; ++fs) {
     const uint32_t f = fs % kFifo, k = fs / kFifo;
@@ -1559,6 +1655,14 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
     if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
     if (lane == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[f].t_sstart = gtimer();
     __syncwarp();
+    if (TC && P.att_grp && in.op == MK_OP_ATTN) {
+      switch (P.qpg) {
+        case 1: storer_attn_grp<1>(P, S, in, lane, epoch); break;
+        case 2: storer_attn_grp<2>(P, S, in, lane, epoch); break;
+        default: storer_attn_grp<4>(P, S, in, lane, epoch); break;
+      }
+      __syncwarp();
+    }
     storer_epilogue(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.iempty[f]);
@@ -1674,7 +1778,7 @@ DEVI void megakernel_body(const KParams &P) {
     }
     __syncwarp();
   } else if (warp == 1) {
-    storer(P, S, epoch, lane);
+    storer<TC>(P, S, epoch, lane);
   } else {
     compute<TC>(P, S, epoch, warp - 2, lane);
   }
