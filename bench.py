@@ -43,6 +43,8 @@ def args_():
     p.add_argument("--config", default=DEFAULT, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--sched", default="static", choices=["dynamic", "static", "hybrid"])
+    p.add_argument("--attn-chunk", type=int, default=0,
+                   help="mk_config.attn_chunk (0: the planner's choice)")
     p.add_argument("--l2kb", type=int, default=0,
                    help="mk_config.l2_prefetch_kb: KB per block prefetched into L2 ahead of the ring")
     p.add_argument("--stream", action="store_true",
@@ -342,7 +344,7 @@ def run_mine(a):
                                                  "hybrid": mk.MK_SCHED_HYBRID,
                                                  "dynamic": mk.MK_SCHED_DYNAMIC}[a.sched],
                          flags=(mk.MK_FLAG_TRACE if a.trace else 0) | (mk.MK_FLAG_STREAM_B1 if a.stream else 0),
-                         l2_prefetch_kb=a.l2kb)
+                         l2_prefetch_kb=a.l2kb, attn_chunk=a.attn_chunk)
     plan = mk.mk_plan(cfg)
     info = mk.mk_plan_info(plan)
     mk.mk_load_weights(plan, {"embed": up(weights["embed"]), "final_norm": up(weights["final_norm"]),

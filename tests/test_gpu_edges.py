@@ -92,14 +92,18 @@ def test_batch1_edges(case, stream):
 
 
 # batch > 1: tensor-core kernel.  tiny_b4_ragged, max_ctx 128 (64-position
-# chunks): sequence 0 from position 0, 1 across the chunk boundary at 64, 2 up
-# to max_ctx - 1, 3 inside chunk 0.
+# chunks forced): sequence 0 from position 0, 1 across the chunk boundary at
+# 64, 2 up to max_ctx - 1, 3 inside chunk 0.
 BATCHED = {
-    "tiny_b4": ("tiny_b4_ragged", [0, 60, 120, 31], 128, 8, 64, {}),
+    "tiny_b4": ("tiny_b4_ragged", [0, 60, 120, 31], 128, 8, 64, {"attn_chunk": 64}),
     # Llama-1B batch 8, max_ctx 4096, 256-position chunks (one key page):
     # sequences from 0, across 256, 1024, 2048 and 3072, and up to 4095
     "llama1b_b8": ("llama1b_b8_ragged", [0, 255, 254, 1022, 2047, 4093, 129, 3071], 4096, 3,
-                   256, {}),
+                   256, {"attn_chunk": 256}),
+    # the same with the planner's own chunking (384 positions: one and a half
+    # key pages, so chunks straddle page boundaries at 256, 768, ...)
+    "llama1b_b8_auto": ("llama1b_b8_ragged", [0, 383, 384, 767, 2047, 4093, 255, 3071], 4096,
+                        3, 384, {}),
     # batch 32 (16 KB pages: 128 keys per page) with 256-position chunks, so
     # a chunk's keys and values span two pages each: sequences at 0, across
     # the page boundary inside a chunk (128), across chunk boundaries (256),
