@@ -251,7 +251,13 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     att_bytes = (uint32_t)(kComputeWarps * qpg * (d + 2) + kComputeWarps * P.att_lmax) * 4;
   // tensor-core plans also gather a split block's slice sums here (MR x B)
   if (P.tc) att_bytes = std::max<uint32_t>(att_bytes, 128u * (uint32_t)B * 4u);
-  uint32_t rel_att = take(att_bytes, 16);
+  // Tensor-core plans whose B operand has no zero rows (2B columns exactly)
+  // keep the grouped attention scratch inside the B-operand slots: those are
+  // idle between projections (every MMA of a tile has completed before its
+  // accumulator is read), and a projection's staging starts only after the
+  // attention chunk before it has passed its last barrier.
+  const bool att_in_xs = P.att_grp && P.tc_nb == 2u * (uint32_t)B;
+  uint32_t rel_att = take(att_in_xs ? 0u : att_bytes, 16);
   uint32_t rel_sat = take((uint32_t)L * (nkv + 4) * 4, 16);  // the waited counters
   uint32_t rel_pos = take(2 * kMaxBatch * 4, 16);
   uint32_t rel_rope = take(B * d * 4, 16);
@@ -268,6 +274,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
       if (op != MK_OP_ATTN)
         xs_floats = std::max<uint32_t>(xs_floats, kTcBufs * P.geom[op].kc * P.tc_nb / 2);
+  if (att_in_xs) xs_floats = std::max<uint32_t>(xs_floats, att_bytes / 4);
   uint32_t rel_xs = take((xs_floats + kComputeWarps) * 4, 16);
   uint32_t bars_max = (2 * kMaxRing + 4 * kFifo + 4 + 2 * kTcBufs) * 8;
   uint32_t rel_bars = take(bars_max, 8);
@@ -307,7 +314,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.off_fifo = ring + rel_fifo;
   P.off_meta = ring + rel_meta;
   P.off_res = ring + rel_res;
-  P.off_att = ring + rel_att;
+  P.off_att = ring + (att_in_xs ? rel_xs : rel_att);
   P.off_sat = ring + rel_sat;
   P.off_pos = ring + rel_pos;
   P.off_rope = ring + rel_rope;
