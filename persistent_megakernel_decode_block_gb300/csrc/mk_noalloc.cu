@@ -64,33 +64,58 @@ __device__ __forceinline__ void chunk_range(int pos, int nch, int c, int &p0, in
 }
 
 // One chunk of one KV group of one sequence: partial {m[qpg], l[qpg], o[qpg][d]}.
+// 128 threads.  Scores: a warp reads DD/8 lanes' 16 bytes of each of
+// 256/DD consecutive key rows at a time (whole rows, contiguous), every lane
+// dots its 8 dimensions with every head's query and a butterfly over the
+// row's lanes finishes each score.  Values: warp w takes rows w, w + 4, ...,
+// each lane DD/32 consecutive dimensions of a row (one contiguous row per
+// warp step), all heads at once; the four warps' sums meet in shared memory.
+template <int DD>
 __global__ void noalloc_attn_partial(const float *q, const uint16_t *kc, const uint16_t *vc,
                                      const int32_t *positions, float *part, int nq, int nkv,
-                                     int d, int max_ctx, int nch, int ch, float scale) {
+                                     int max_ctx, int nch, int ch, float scale) {
+  constexpr int LPP = DD / 8, RPS = 32 / LPP, DPL = DD / 32, MAXQ = 8;
   extern __shared__ float sm[];
   const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int qpg = nq / nkv, PS = 2 * qpg + qpg * d;
-  float *qs = sm, *s = sm + qpg * d;
+  const int qpg = nq / nkv, PS = 2 * qpg + qpg * DD;
+  float *qs = sm, *s = qs + qpg * DD, *po = s + qpg * ch;  // po: [4][qpg][DD]
   float *dst = part + (((size_t)b * nkv + g) * nch + c) * PS;
   const int pos = positions[b];
   int p0 = 0, p1 = 0;
   if (pos >= 0 && pos < max_ctx) chunk_range(pos, nch, c, p0, p1);
   const int n = p1 - p0;
-  for (int i = threadIdx.x; i < qpg * d; i += blockDim.x)
-    qs[i] = q[((size_t)b * nq + (size_t)g * qpg) * d + i];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < qpg * DD; i += blockDim.x)
+    qs[i] = q[((size_t)b * nq + (size_t)g * qpg) * DD + i] * scale;
   __syncthreads();
-  const size_t base = (((size_t)b * nkv + g) * max_ctx + p0) * d;
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const uint16_t *kr = kc + base + (size_t)j * d;
+  const size_t base = (((size_t)b * nkv + g) * max_ctx + p0) * DD;
+  const int part8 = (lane % LPP) * 8;
+  for (int j0 = warp * RPS; j0 < n; j0 += 4 * RPS) {
+    const int j = j0 + lane / LPP;
+    float k8[8];
+    if (j < n) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(kc + base + (size_t)j * DD + part8);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        k8[2 * t] = __uint_as_float(u[t] << 16);
+        k8[2 * t + 1] = __uint_as_float(u[t] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) k8[t] = 0.f;
+    }
     for (int h = 0; h < qpg; ++h) {
-      float acc = 0.f;
-      for (int k = 0; k < d; ++k) acc = fmaf(qs[h * d + k], bf(kr[k]), acc);
-      s[h * ch + j] = acc * scale;
+      float a = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) a = fmaf(qs[h * DD + part8 + t], k8[t], a);
+#pragma unroll
+      for (int o = LPP / 2; o; o >>= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+      if (j < n && lane % LPP == 0) s[h * ch + j] = a;
     }
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  for (int h = warp; h < qpg; h += nwarps) {
+  for (int h = warp; h < qpg; h += 4) {
     float m = -INFINITY;
     for (int j = lane; j < n; j += 32) m = fmaxf(m, s[h * ch + j]);
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -101,17 +126,42 @@ __global__ void noalloc_attn_partial(const float *q, const uint16_t *kc, const u
       l += p;
     }
     for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    __syncwarp();
-    for (int k = lane; k < d; k += 32) {
-      float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(s[h * ch + j], bf(vc[base + (size_t)j * d + k]), acc);
-      dst[2 * qpg + h * d + k] = acc;
-    }
     if (lane == 0) {
       dst[h] = m;
       dst[qpg + h] = l;
     }
   }
+  __syncthreads();
+  float acc[MAXQ][DPL];
+#pragma unroll
+  for (int h = 0; h < MAXQ; ++h)
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) acc[h][k] = 0.f;
+  for (int j = warp; j < n; j += 4) {
+    const uint16_t *vr = vc + base + (size_t)j * DD + lane * DPL;
+    float v[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; k += 2) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(vr + k);
+      v[k] = __uint_as_float(w << 16);
+      v[k + 1] = __uint_as_float(w & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int h = 0; h < MAXQ; ++h)
+      if (h < qpg) {
+        const float p = s[h * ch + j];
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(p, v[k], acc[h][k]);
+      }
+  }
+#pragma unroll
+  for (int h = 0; h < MAXQ; ++h)
+    if (h < qpg)
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) po[((size_t)warp * qpg + h) * DD + lane * DPL + k] = acc[h][k];
+  __syncthreads();
+  for (int i = tid; i < qpg * DD; i += blockDim.x)
+    dst[2 * qpg + i] = (po[i] + po[qpg * DD + i]) + (po[2 * qpg * DD + i] + po[3 * qpg * DD + i]);
 }
 
 // Log-sum-exp merge of a group's chunk partials into out[b][(g*qpg + h)*d + k];
@@ -167,11 +217,16 @@ extern "C" MK_API int mk_attention_noalloc(const float *q, const void *k_cache,
   int rc = scratch_for_current_device(&scratch);
   if (rc != MK_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t smem = (size_t)(qpg * head_dim + qpg * ch) * sizeof(float);
-  noalloc_attn_partial<<<dim3(nch, n_kv_heads, batch), 128, smem, s>>>(
-      q, static_cast<const uint16_t *>(k_cache), static_cast<const uint16_t *>(v_cache),
-      positions, scratch, n_q_heads, n_kv_heads, head_dim, max_ctx, nch, ch,
-      (float)(1.0 / sqrt((double)head_dim)));
+  const size_t smem = (size_t)(qpg * head_dim + qpg * ch + 4 * qpg * head_dim) * sizeof(float);
+  const float scale = (float)(1.0 / sqrt((double)head_dim));
+  const uint16_t *kc = static_cast<const uint16_t *>(k_cache);
+  const uint16_t *vc = static_cast<const uint16_t *>(v_cache);
+  if (head_dim == 64)
+    noalloc_attn_partial<64><<<dim3(nch, n_kv_heads, batch), 128, smem, s>>>(
+        q, kc, vc, positions, scratch, n_q_heads, n_kv_heads, max_ctx, nch, ch, scale);
+  else
+    noalloc_attn_partial<128><<<dim3(nch, n_kv_heads, batch), 128, smem, s>>>(
+        q, kc, vc, positions, scratch, n_q_heads, n_kv_heads, max_ctx, nch, ch, scale);
   if (cudaGetLastError() != cudaSuccess) return MK_ERR_LAUNCH;
   noalloc_attn_merge<<<dim3(n_kv_heads, batch), 128, 0, s>>>(
       scratch, positions, out, n_q_heads, n_kv_heads, head_dim, max_ctx, nch);
