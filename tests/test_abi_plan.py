@@ -245,12 +245,38 @@ def test_fault_flag_makes_one_target_unreachable():
 
 @pytest.mark.parametrize("field, value", [
     ("hidden", 200), ("ffn_dim", 300), ("n_q_heads", 6), ("head_dim", 96), ("batch", 0),
-    ("batch", 17), ("max_ctx", 100), ("page_bytes", 1000), ("n_layers", 0), ("attn_chunk", 24),
+    ("batch", 17), ("batch", 24), ("batch", 64), ("max_ctx", 100), ("page_bytes", 1000),
+    ("n_layers", 0), ("attn_chunk", 24), ("sched_mode", 3),
 ])
 def test_invalid_configs_are_rejected(field, value):
     w = WORKLOADS["tiny"]
     cfg = mk.make_config(w["model"], 1, 128, num_sms=8, flags=mk.MK_FLAG_HOST_ONLY)
     setattr(cfg, field, value)
+    with pytest.raises(mk.MkError) as e:
+        mk.mk_plan(cfg)
+    assert e.value.code == mk.MK_ERR_CONFIG
+
+
+def test_planner_choices_for_the_larger_batch_mode_and_the_hybrid_schedule():
+    w = WORKLOADS["llama1b_b32_ragged"]
+    # batch 32: 16 KB pages by default; 32 KB pages would need more staging
+    # threads than the compute warps have, so that plan is refused
+    p = mk.mk_plan(mk.make_config(w["model"], 32, 4160, num_sms=152, flags=mk.MK_FLAG_HOST_ONLY))
+    try:
+        info = mk.mk_plan_info(p)
+        assert info["page_bytes"] == 16384 and info["kernel"] == 1
+        assert info["attn_chunk"] == 384  # grouped chunks: three 16 KB key pages
+    finally:
+        mk.mk_destroy(p)
+    cfg = mk.make_config(w["model"], 32, 4160, num_sms=152, page_bytes=32768,
+                         flags=mk.MK_FLAG_HOST_ONLY)
+    with pytest.raises(mk.MkError) as e:
+        mk.mk_plan(cfg)
+    assert e.value.code == mk.MK_ERR_CONFIG
+    # the hybrid schedule does not run the per-warp stream kernel
+    t = WORKLOADS["tiny"]
+    cfg = mk.make_config(t["model"], 1, 128, num_sms=8, sched_mode=mk.MK_SCHED_HYBRID,
+                         flags=mk.MK_FLAG_HOST_ONLY | mk.MK_FLAG_STREAM_B1)
     with pytest.raises(mk.MkError) as e:
         mk.mk_plan(cfg)
     assert e.value.code == mk.MK_ERR_CONFIG
