@@ -373,16 +373,33 @@ DEVI bool stage_input(const KParams &P, const Smem &S, const mk_instr &in, int c
   const int emb = in.op == MK_OP_QKV && (in.flags & 1);
   const float *src = in.op == MK_OP_OPROJ ? P.attn : P.x;
   float ss = 0.f;
-  for (uint32_t i = (uint32_t)(cw * 32 + lane) * 4; i < K; i += kComputeWarps * 32 * 4) {
-    float4 v;
-    if (emb) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2 *>(P.embed + (size_t)S.tok[0] * P.H + i));
-      v = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-    } else {
-      v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+  // every load of a thread is issued before the first is used, so the
+  // staging costs one round trip to L2 (KS loads of 4 values per thread
+  // cover K up to KS * 14 * 32 * 4 = 5376; a longer K takes more batches)
+  constexpr int KS = 3;
+  constexpr uint32_t kStride = kComputeWarps * 32 * 4;
+  for (uint32_t i0 = (uint32_t)(cw * 32 + lane) * 4; i0 < K; i0 += KS * kStride) {
+    float4 v[KS];
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+      const uint32_t i = i0 + t * kStride;
+      v[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < K) {
+        if (emb) {
+          const uint2 w =
+              __ldg(reinterpret_cast<const uint2 *>(P.embed + (size_t)S.tok[0] * P.H + i));
+          v[t] = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        } else {
+          v[t] = __ldcg(reinterpret_cast<const float4 *>(src + i));
+        }
+      }
     }
-    *reinterpret_cast<float4 *>(S.xs + i) = v;
-    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+#pragma unroll
+    for (int t = 0; t < KS; ++t) {
+      const uint32_t i = i0 + t * kStride;
+      if (i < K) *reinterpret_cast<float4 *>(S.xs + i) = v[t];
+      ss = fmaf(v[t].x, v[t].x, fmaf(v[t].y, v[t].y, fmaf(v[t].z, v[t].z, fmaf(v[t].w, v[t].w, ss))));
+    }
   }
   ss = warp_sum(ss);
   if (lane == 0) S.xs[K + cw] = ss;
