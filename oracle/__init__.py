@@ -22,6 +22,16 @@ _D = ctypes.POINTER(ctypes.c_double)
 _U16 = ctypes.POINTER(ctypes.c_uint16)
 
 
+Q8_KINDS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+class _Q8(ctypes.Structure):
+    # codes per kind (wq ...), then scales per kind (sq ...), then the LM head
+    _fields_ = [(k, ctypes.POINTER(ctypes.c_void_p)) for k in Q8_KINDS] + [
+        ("s" + k[1:], ctypes.POINTER(ctypes.c_void_p)) for k in Q8_KINDS] + [
+        ("lm", ctypes.c_void_p), ("s_lm", ctypes.c_void_p)]
+
+
 class _Model(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int), ("H", ctypes.c_int), ("nq", ctypes.c_int),
                 ("nkv", ctypes.c_int), ("d", ctypes.c_int), ("F", ctypes.c_int),
@@ -29,7 +39,8 @@ class _Model(ctypes.Structure):
                 ("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
                 ("lm_head", ctypes.c_void_p)] + [
         (k, ctypes.POINTER(ctypes.c_void_p)) for k in
-        ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")]
+        ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up", "w_down")] + [
+        ("q8", ctypes.POINTER(_Q8))]
 
 
 class _Shape(ctypes.Structure):
@@ -48,6 +59,10 @@ def lib():
             "or_bf16_rne": (ctypes.c_uint16, [dbl]),
             "or_rmsnorm": (None, [i, vp, vp, dbl, vp]),
             "or_matvec": (None, [i, i, vp, vp, vp]),
+            "or_e4m3_to_double": (dbl, [ctypes.c_uint8]),
+            "or_e4m3_rne": (ctypes.c_uint8, [dbl]),
+            "or_quantize_rows": (None, [i, i, vp, vp, vp]),
+            "or_matvec_q8": (None, [i, i, vp, vp, vp, vp]),
             "or_rope": (None, [i, dbl, dbl, vp]),
             "or_silu": (dbl, [dbl]),
             "or_attention": (None, [i, i, vp, vp, vp, vp]),
@@ -100,6 +115,33 @@ def matvec(W, x):
     return y
 
 
+def e4m3_to_double(c):
+    return float(lib().or_e4m3_to_double(int(c)))
+
+
+def e4m3_rne(v):
+    return int(lib().or_e4m3_rne(float(v)))
+
+
+def quantize_rows(W):
+    """FP8 form of a bf16 matrix [M][K]: (E4M3 codes uint8 [M][K], float32
+    row scales [M])."""
+    W = _u16(W)
+    M, K = W.shape
+    Q = np.empty((M, K), np.uint8)
+    s = np.empty(M, np.float32)
+    lib().or_quantize_rows(M, K, W.ctypes.data, Q.ctypes.data, s.ctypes.data)
+    return Q, s
+
+
+def matvec_q8(Q, s, x):
+    Q, s, x = np.ascontiguousarray(Q, np.uint8), np.ascontiguousarray(s, np.float32), _f64(x)
+    M, K = Q.shape
+    y = np.empty(M)
+    lib().or_matvec_q8(M, K, Q.ctypes.data, s.ctypes.data, x.ctypes.data, y.ctypes.data)
+    return y
+
+
 def rope(z, pos, theta):
     z = _f64(z).copy()
     lib().or_rope(z.size, float(pos), float(theta), z.ctypes.data)
@@ -127,7 +169,9 @@ class Model:
     """Holds a model's bf16 weights (numpy uint16, PyTorch layout) and its own
     KV cache, and runs oracle decode steps on them."""
 
-    def __init__(self, cfg, weights, batch, max_ctx, kcache, vcache):
+    def __init__(self, cfg, weights, batch, max_ctx, kcache, vcache, fp8=False):
+        """fp8: every projection and the LM head in their FP8 form
+        (quantize_rows); the token lookup and the norms stay bf16."""
         self.cfg, self.w, self.B, self.max_ctx = cfg, weights, batch, max_ctx
         self.k = np.array(kcache, dtype=np.uint16, copy=True, order="C")
         self.v = np.array(vcache, dtype=np.uint16, copy=True, order="C")
@@ -150,6 +194,21 @@ class Model:
         for kind in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "w_gate", "w_up",
                      "w_down"):
             setattr(m, kind, arr(kind))
+        if fp8:
+            q8 = _Q8()
+            for kind in Q8_KINDS:
+                sk = "s" + kind[1:]
+                qs = [quantize_rows(weights["layers"][l][kind]) for l in range(L)]
+                self._keep.append(qs)
+                for field, j in ((kind, 0), (sk, 1)):
+                    ptrs = (ctypes.c_void_p * L)(*[qs[l][j].ctypes.data for l in range(L)])
+                    self._keep.append(ptrs)
+                    setattr(q8, field, ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)))
+            lm = weights["lm_head"] if weights["lm_head"] is not None else weights["embed"]
+            self.q8_lm = quantize_rows(lm)
+            q8.lm, q8.s_lm = self.q8_lm[0].ctypes.data, self.q8_lm[1].ctypes.data
+            self._q8 = q8
+            m.q8 = ctypes.pointer(q8)
         self._m = m
 
     def step(self, tokens, positions):

@@ -67,6 +67,77 @@ void or_matvec(int M, int K, const uint16_t *W, const double *x, double *y) {
   }
 }
 
+/* FP8 E4M3 (the OCP 8-bit floating-point format, variant without
+   infinities): sign, 4 exponent bits with bias 7, 3 mantissa bits.  Exponent
+   field 0 holds the subnormals m/8 * 2^-6; fields 1..15 hold
+   (1 + m/8) * 2^(e-7), except field 15 with mantissa 7, which is NaN, so the
+   largest finite magnitude is 1.75 * 2^8 = 448.  Code -> value, exact. */
+double or_e4m3_to_double(uint8_t c) {
+  int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double a;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    a = ldexp((double)m, -9);
+  else
+    a = ldexp(8.0 + (double)m, e - 10);
+  return sgn ? -a : a;
+}
+
+/* Value -> code: round to nearest, ties to even, magnitudes past the
+   largest finite one saturate to +-448 (no NaN is produced for a finite
+   input).  The grid spacing is 2^-9 below 2^-6 (subnormals) and 2^(e-3)
+   in the binade [2^e, 2^(e+1)). */
+uint8_t or_e4m3_rne(double v) {
+  uint8_t sgn = signbit(v) ? 0x80 : 0;
+  double a = fabs(v);
+  if (isnan(v)) return 0x7F;
+  if (a >= 448.0) return sgn | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    double q = nearbyint(ldexp(a, 9)); /* multiples of 2^-9; 8 -> smallest normal */
+    return sgn | (uint8_t)q;
+  }
+  int E;
+  frexp(a, &E);           /* a = f 2^E, 0.5 <= f < 1: binade e = E - 1 */
+  int e = E - 1;
+  double q = nearbyint(ldexp(a, 3 - e)); /* 8 .. 16 */
+  if (q >= 16.0) {
+    q = 8.0;
+    e += 1;
+  }
+  return sgn | (uint8_t)(((e + 7) << 3) | ((int)q - 8));
+}
+
+/* Per-row scaled FP8 quantisation of W [M][K] (bf16): scale_r = amax_r / 448
+   in float (1 when the row is zero), code_rk = e4m3(w_rk / scale_r) with the
+   division in float, so the largest magnitude of each row maps to +-448. */
+void or_quantize_rows(int M, int K, const uint16_t *W, uint8_t *Q, float *scale) {
+  for (int r = 0; r < M; ++r) {
+    const uint16_t *w = W + (size_t)r * K;
+    float amax = 0.0f;
+    for (int k = 0; k < K; ++k) {
+      float a = (float)fabs(or_bf16_to_double(w[k]));
+      if (a > amax) amax = a;
+    }
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    scale[r] = s;
+    for (int k = 0; k < K; ++k) {
+      float v = (float)or_bf16_to_double(w[k]) / s;
+      Q[(size_t)r * K + k] = or_e4m3_rne((double)v);
+    }
+  }
+}
+
+/* y = W x for the FP8 weights W_rk = e4m3(Q_rk) * scale_r. */
+void or_matvec_q8(int M, int K, const uint8_t *Q, const float *scale, const double *x,
+                  double *y) {
+  for (int r = 0; r < M; ++r) {
+    const uint8_t *q = Q + (size_t)r * K;
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k) acc += or_e4m3_to_double(q[k]) * (double)scale[r] * x[k];
+    y[r] = acc;
+  }
+}
+
 /* Rotary position embedding, rotate-half convention (HF Llama): for
    i < d/2 the pair (z_i, z_{i+d/2}) is rotated by the angle
    pos * theta^(-2i/d). */
@@ -127,8 +198,18 @@ int or_argmax(int n, const double *v) {
  * RoPE on q and k at p; store bf16(k), bf16(v) at p; for every q head h of
  * group g = h / (nq/nkv): o_h = attention(q_h, K[g][0..p], V[g][0..p]);
  * x += Wo concat(o); y = RMSNorm(x) g2; x += Wd (silu(Wg y) * (Wu y));
- * finally logits = W_lm (RMSNorm(x) g_f), W_lm = E when tied.
+ * finally logits = W_lm (RMSNorm(x) g_f), W_lm = E when tied.  With m->q8
+ * every projection (and W_lm) is its FP8 form instead (or_matvec_q8).
  * Returns 0, or -1 on a bad argument. */
+/* projection `w` of layer l: bf16, or FP8 codes with row scales `sc` */
+#define MV(M_, K_, w, sc, x_, y_)                                              \
+  do {                                                                         \
+    if (m->q8)                                                                 \
+      or_matvec_q8((M_), (K_), m->q8->w[l], m->q8->sc[l], (x_), (y_));         \
+    else                                                                       \
+      or_matvec((M_), (K_), m->w[l], (x_), (y_));                              \
+  } while (0)
+
 int or_decode_step(const or_model *m, int B, int max_ctx, uint16_t *kc, uint16_t *vc,
                    const int32_t *tokens, const int32_t *positions, double *logits) {
   const int H = m->H, nq = m->nq, nkv = m->nkv, d = m->d, F = m->F, V = m->V, L = m->L;
@@ -153,9 +234,9 @@ int or_decode_step(const or_model *m, int B, int max_ctx, uint16_t *kc, uint16_t
     for (int i = 0; i < H; ++i) x[i] = or_bf16_to_double(m->embed[(size_t)tok * H + i]);
     for (int l = 0; l < L; ++l) {
       or_rmsnorm(H, x, m->attn_norm[l], m->eps, y);
-      or_matvec(nq * d, H, m->wq[l], y, q);
-      or_matvec(nkv * d, H, m->wk[l], y, k);
-      or_matvec(nkv * d, H, m->wv[l], y, v);
+      MV(nq * d, H, wq, sq, y, q);
+      MV(nkv * d, H, wk, sk, y, k);
+      MV(nkv * d, H, wv, sv, y, v);
       for (int h = 0; h < nq; ++h) or_rope(d, (double)p, m->theta, q + (size_t)h * d);
       for (int g = 0; g < nkv; ++g) or_rope(d, (double)p, m->theta, k + (size_t)g * d);
       for (int g = 0; g < nkv; ++g) {
@@ -170,17 +251,20 @@ int or_decode_step(const or_model *m, int B, int max_ctx, uint16_t *kc, uint16_t
         size_t base = (((size_t)l * B + b) * nkv + g) * (size_t)max_ctx * d;
         or_attention(d, p + 1, q + (size_t)h * d, kc + base, vc + base, o + (size_t)h * d);
       }
-      or_matvec(H, nq * d, m->wo[l], o, t);
+      MV(H, nq * d, wo, so, o, t);
       for (int i = 0; i < H; ++i) x[i] += t[i];
       or_rmsnorm(H, x, m->mlp_norm[l], m->eps, y);
-      or_matvec(F, H, m->w_gate[l], y, gt);
-      or_matvec(F, H, m->w_up[l], y, up);
+      MV(F, H, w_gate, s_gate, y, gt);
+      MV(F, H, w_up, s_up, y, up);
       for (int i = 0; i < F; ++i) gt[i] = or_silu(gt[i]) * up[i];
-      or_matvec(H, F, m->w_down[l], gt, t);
+      MV(H, F, w_down, s_down, gt, t);
       for (int i = 0; i < H; ++i) x[i] += t[i];
     }
     or_rmsnorm(H, x, m->final_norm, m->eps, y);
-    or_matvec(V, H, m->lm_head ? m->lm_head : m->embed, y, logits + (size_t)b * V);
+    if (m->q8)
+      or_matvec_q8(V, H, m->q8->lm, m->q8->s_lm, y, logits + (size_t)b * V);
+    else
+      or_matvec(V, H, m->lm_head ? m->lm_head : m->embed, y, logits + (size_t)b * V);
   }
   free(x);
   free(y);
