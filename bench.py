@@ -209,10 +209,12 @@ def cpu_facts():
     return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
 
 
-def time_workload(mk, torch, dev, name, a):
+def time_workload(mk, torch, dev, name, a, fp8=False):
     """Another workload, timed as the headline one (same steps and warm-up,
     static lists, device-resident inputs, CUDA events on the launching
-    stream, clocks sampled): ms/step, passes/s and roofline fraction."""
+    stream, clocks sampled): ms/step, passes/s and roofline fraction.  fp8:
+    the same workload with FP8 weights (MK_FLAG_FP8_WEIGHTS); its roofline
+    bytes are the FP8 codes and row scales."""
     w = WORKLOADS[name]
     m, B = w["model"], w["batch"]
     ctx, mctx = contexts(name, a.seed), max_ctx(name, a.seed)
@@ -223,7 +225,8 @@ def time_workload(mk, torch, dev, name, a):
     def up(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev)
 
-    plan = mk.mk_plan(mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC))
+    plan = mk.mk_plan(mk.make_config(m, B, mctx, sched_mode=mk.MK_SCHED_STATIC,
+                                     flags=mk.MK_FLAG_FP8_WEIGHTS if fp8 else 0))
     try:
         info = mk.mk_plan_info(plan)
         mk.mk_load_weights(plan, {"embed": up(weights["embed"]),
@@ -266,9 +269,11 @@ def time_workload(mk, torch, dev, name, a):
                 "tokens_per_s": 1000.0 * B / ms,
                 "roofline": {"achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "bytes_per_step": bytes_step,
-                             "traffic": recorded_traffic(name),
+                             "traffic": None if fp8 else recorded_traffic(name),
                              "peak_kind": peak_kind + " hbm_gbs"},
-                "kernel": "mk_megakernel_tc" if B > 1 else "mk_megakernel",
+                "kernel": "mk_megakernel_tc" if B > 1 else "mk_megakernel_q8" if fp8
+                          else "mk_megakernel",
+                "weights": "fp8 e4m3, one scale per row" if fp8 else "bf16",
                 "clocks": clocks.summary()}
     finally:
         mk.mk_destroy(plan)
@@ -451,6 +456,10 @@ def run_mine(a):
         extra["workloads"] = {o: time_workload(mk, torch, dev, o, a) for o in
                               ("llama1b_ctx8192", "llama1b_b8_ragged", "llama1b_b32_ragged",
                                "llama8b_ctx2048")}
+        # the same headline workload with FP8 weights (a lower-precision mode,
+        # not the headline: its bytes per step are about half)
+        extra["workloads"]["llama1b_ctx1024_fp8"] = time_workload(mk, torch, dev, DEFAULT, a,
+                                                                  fp8=True)
     if rank != 0:
         return
     line = {

@@ -73,6 +73,16 @@ extern "C" {
                                    a private ring of per-lane async copies, instead of the
                                    block's shared page ring fed by the loader warp's bulk
                                    copies (the default); an alternative kept for comparison */
+#define MK_FLAG_FP8_WEIGHTS 0x10u /* batch 1, shared page ring: every projection and the LM
+                                     head streamed as FP8 E4M3 codes with one float scale per
+                                     output row (scale = row amax / 448, code = E4M3 of w /
+                                     scale, round to nearest even, saturating), quantised by
+                                     mk_load_weights from the bf16 weights; the embedding
+                                     lookup, the norms and the KV cache stay bf16.  The pages'
+                                     "lower precision" lever (« Résumé exécutif », "Les six
+                                     leviers"); results differ from bf16 by the weights'
+                                     quantisation.  MK_ERR_CONFIG for batch > 1 or with
+                                     MK_FLAG_STREAM_B1 */
 
 #define MK_SCHED_DYNAMIC 0 /* global work queue, one atomic claim per instruction */
 #define MK_SCHED_STATIC 1  /* per-SM lists, round-robin over the queue order */
@@ -153,11 +163,13 @@ typedef struct mk_plan_info_s {
   uint32_t attn_nchunk;     /* attention chunks per (sequence, group) */
   uint32_t attn_chunk;      /* max positions per chunk */
   uint64_t arena_bytes;     /* re-tiled weights held by the plan */
-  uint64_t weight_bytes;    /* algorithmic weight bytes streamed per step */
+  uint64_t weight_bytes;    /* algorithmic weight bytes streamed per step (FP8 plans: codes
+                               and row scales) */
   uint32_t warp_ring_slots; /* MK_FLAG_STREAM_B1 plans: 512-byte slots in each compute
                                warp's ring (0: the plan uses the shared page ring) */
   uint32_t kernel;          /* 0 shared page ring (batch 1, the default), 1 tensor cores
-                               (batch > 1), 2 per-warp streams (batch 1, MK_FLAG_STREAM_B1) */
+                               (batch > 1), 2 per-warp streams (batch 1, MK_FLAG_STREAM_B1),
+                               3 shared page ring with FP8 weights (MK_FLAG_FP8_WEIGHTS) */
 } mk_plan_info_t;
 
 /* Weights in PyTorch layout ([out, in] row-major, bf16 bit patterns), as host

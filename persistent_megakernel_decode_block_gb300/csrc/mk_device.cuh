@@ -184,6 +184,7 @@ struct Smem {
   uint64_t *dmask;     // attention re-deal: per chunk, the sequences it has work for
   uint32_t *dpre;      // and the prefix count of (chunk, sequence) pairs with work
   volatile int *misc;  // [0] bail, [1] bad input
+  float *wsc;          // FP8 plans: the storer's copy of the current tile's row scales
 };
 
 static_assert(sizeof(Smem) <= kMiscDescBytes, "pointer table larger than its slot");
@@ -221,6 +222,7 @@ DEVI Smem make_smem(const KParams &P, uint8_t *base) {
   S.dpre = reinterpret_cast<uint32_t *>(S.dmask + kMaxDealChunks);
   S.rbuf = reinterpret_cast<float *>(base + P.off_rbuf);
   S.xs = reinterpret_cast<float *>(base + P.off_xs);
+  S.wsc = reinterpret_cast<float *>(base + P.off_wsc);
   S.wring = base + P.off_wring;
   return S;
 }
@@ -409,6 +411,9 @@ DEVI void finish_entry(const KParams &P, const Smem &S, uint32_t fs, int cw, int
 }
 
 // --------------------------------------------------------------- storer ----
+// Q8: FP8 weights; a tile row's sum is multiplied by the row's scale (the
+// storer copied the tile's scales into S.wsc while the compute warps ran).
+template <bool Q8 = false>
 DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
                           const SlotMeta &meta, const float *res, int lane, uint32_t epoch) {
   const int B = P.B, d = P.d;
@@ -416,6 +421,7 @@ DEVI void storer_epilogue(const KParams &P, const Smem &S, const mk_instr &in,
   auto val = [&](uint32_t r, int b) {
     float v = 0.f;
     for (uint32_t s = 0; s < G.NS; ++s) v += res[(r * G.NS + s) * B + b];
+    if (Q8) v *= S.wsc[r];
     return v;
   };
   uint32_t *ctr = P.ctr;

@@ -89,6 +89,8 @@ struct KParams {
   uint32_t ring_pages, page_bytes;
   uint32_t off_bars, off_fifo, off_meta, off_res, res_floats, off_att, off_sat, off_pos,
       off_rope, off_normr, off_misc, off_rbuf, off_xs, off_wring, off_deal, smem_total;
+  int32_t fp8;       // batch 1: FP8 E4M3 weight codes with one scale per row (MK_FLAG_FP8_WEIGHTS)
+  uint32_t off_wsc;  // FP8 plans: the storer's row-scale buffer in shared memory
 };
 
 // per FIFO slot metadata written by the loader
@@ -102,6 +104,12 @@ constexpr int kTraceWords = 10;  // u64 per instruction in the trace buffer
 
 #ifdef __CUDACC__
 cudaError_t set_megakernel_smem(uint32_t bytes);
+cudaError_t launch_row_scale(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             const uint64_t *scaletab, uint32_t nrows, uint32_t K,
+                             cudaStream_t stream);
+cudaError_t launch_retile_q8(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             const uint64_t *rowtab, const uint64_t *scaletab, uint32_t nrows,
+                             const OpGeom &g, uint32_t page, cudaStream_t stream);
 cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
                               cudaStream_t stream);
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream);

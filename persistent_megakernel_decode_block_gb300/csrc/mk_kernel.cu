@@ -22,6 +22,11 @@
 // Every wait is bounded by %globaltimer; on expiry the block latches
 // MK_ERR_TIMEOUT, raises a global abort flag that every other wait polls,
 // waits for its own copies in flight and returns.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
 #include "mk_device.cuh"
 
 namespace mk {
@@ -462,6 +467,39 @@ DEVI float dot_item_b1(const uint8_t *item, const XCache &X, int nch, int lane) 
   return (a0 + a1) + (a2 + a3);
 }
 
+// FP8 weights: an item is SW E4M3 codes (one byte each); lane l's eight codes
+// of chunk j are the same columns as in the bf16 item (j 256 + 8 l + t).
+DEVI float2 e4m3x2_to_float2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+
+DEVI float dot_item_q8(const uint8_t *item, const XCache &X, int nch, int lane) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxChunks; ++j)
+    if (j < nch) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(item + j * 256 + lane * 8);
+      const float2 f0 = e4m3x2_to_float2(w.x & 0xFFFFu), f1 = e4m3x2_to_float2(w.x >> 16);
+      const float2 f2 = e4m3x2_to_float2(w.y & 0xFFFFu), f3 = e4m3x2_to_float2(w.y >> 16);
+      a0 = fmaf(f0.x, X.v[j][0], a0);
+      a1 = fmaf(f0.y, X.v[j][1], a1);
+      a2 = fmaf(f1.x, X.v[j][2], a2);
+      a3 = fmaf(f1.y, X.v[j][3], a3);
+      a0 = fmaf(f2.x, X.v[j][4], a0);
+      a1 = fmaf(f2.y, X.v[j][5], a1);
+      a2 = fmaf(f3.x, X.v[j][6], a2);
+      a3 = fmaf(f3.y, X.v[j][7], a3);
+    }
+  return (a0 + a1) + (a2 + a3);
+}
+
+template <bool Q8>
+DEVI float dot_item(const uint8_t *item, const XCache &X, int nch, int lane) {
+  if constexpr (Q8) return dot_item_q8(item, X, nch, lane);
+  else return dot_item_b1(item, X, nch, lane);
+}
+
 // Batch > 1: per-sequence 1/rms at every change of input, shared through
 // shared memory (double-buffered by the change count).
 DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int cw, int lane,
@@ -522,6 +560,7 @@ DEVI bool norm_factors(const KParams &P, const Smem &S, const mk_instr &in, int 
 
 // Batch-1 GEMV of one instruction; X holds the normalised input slice when
 // xkey matches the instruction's input.
+template <bool Q8>
 DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const SlotMeta &meta,
                   float *res, int cw, int lane, XCache &X, bool reload) {
   const OpGeom &G = P.geom[in.op];
@@ -548,8 +587,8 @@ DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const Slo
     // reductions overlap
     for (; active && item + A < it_end; item += 2 * A) {
       const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
-      float a = dot_item_b1(ip, X, G.nch, lane);
-      float c = dot_item_b1(ip + A * G.item_bytes, X, G.nch, lane);
+      float a = dot_item<Q8>(ip, X, G.nch, lane);
+      float c = dot_item<Q8>(ip + A * G.item_bytes, X, G.nch, lane);
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
         a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
@@ -562,7 +601,7 @@ DEVI bool gemv_b1(const KParams &P, const Smem &S, const mk_instr &in, const Slo
     }
     for (; active && item < it_end; item += A) {
       const uint8_t *ip = page + (item - p * G.ipp) * G.item_bytes;
-      const float acc = warp_sum(dot_item_b1(ip, X, G.nch, lane));
+      const float acc = warp_sum(dot_item<Q8>(ip, X, G.nch, lane));
       if (lane == 0) res[item] = acc;
     }
     __syncwarp();
@@ -1500,6 +1539,7 @@ DEVI bool attn_dispatch(const KParams &P, const Smem &S, const mk_instr &in,
 
 // Batch-1 run of consecutive GEMV instructions sharing the register input
 // cache; returns at the first attention or end entry (not consumed).
+template <bool Q8>
 DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t epoch, int cw,
                       int lane, uint32_t &xbar_uses) {
   XCache X;
@@ -1517,7 +1557,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return false;
     if (reload && stages_input(P, in) && !stage_input(P, S, in, cw, lane, xbar_uses))
       return false;
-    if (!gemv_b1(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, reload))
+    if (!gemv_b1<Q8>(P, S, in, meta, S.res + (size_t)f * P.res_floats, cw, lane, X, reload))
       return false;
     finish_entry(P, S, fs, cw, lane);
     ++fs;
@@ -1531,7 +1571,7 @@ DEVI bool run_gemv_b1(const KParams &P, const Smem &S, uint32_t &fs, uint32_t ep
 // GEMV; batch > 1 plans run them on the tensor cores.  The two are separate
 // instantiations (and kernels), so neither's registers are shaped by the
 // other's calls.
-template <bool TC>
+template <bool TC, bool Q8>
 DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int lane) {
   uint32_t att_uses = 0, xbar_uses = 0, key_changes = 0, xkey = 0xFFFFFFFFu, tc_uses = 0;
   uint32_t tc_bseq = 0, fs = 0;
@@ -1545,7 +1585,7 @@ DEVI void compute(const KParams &P, const Smem &S, uint32_t epoch, int cw, int l
       return;
     }
     if (!TC && in.op != MK_OP_ATTN) {
-      if (!run_gemv_b1(P, S, fs, epoch, cw, lane, xbar_uses)) return;
+      if (!run_gemv_b1<Q8>(P, S, fs, epoch, cw, lane, xbar_uses)) return;
       continue;
     }
     if (!ready_entry(P, S, fs, in, meta, epoch, cw, lane)) return;
@@ -1659,7 +1699,16 @@ __device__ __noinline__ void storer_attn_grp(const KParams &P, const Smem &S, co
   if (lane == 0) red_release(P.ctr + (size_t)in.sig2_ctr * kCtrStride, 1u);
 }
 
-template <bool TC>
+// FP8 plans: the row scales of a batch-1 tile follow its pages in the arena
+DEVI void prefetch_scales(const KParams &P, const Smem &S, const mk_instr &in, int lane) {
+  if (in.op == MK_OP_ATTN) return;
+  const uint32_t w = in.op == MK_OP_GATEUP ? 2 * in.nrows : in.nrows;
+  const float *sc =
+      reinterpret_cast<const float *>(P.arena + in.wofs + (uint64_t)in.npages * P.page_bytes);
+  for (uint32_t r = lane; r < w; r += 32) S.wsc[r] = __ldg(sc + r);
+}
+
+template <bool TC, bool Q8>
 DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
   for (uint32_t fs = 0;; ++fs) {
     const uint32_t f = fs % kFifo, k = fs / kFifo;
@@ -1669,6 +1718,7 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
     if (in.op == MK_OP_END) break;
     if (!warp_wait(P, S, &S.rdy[f], k & 1u, kWhereStorer)) break;
     if (!P.tc) prefetch_residual(P, S, in, lane);
+    if (Q8) prefetch_scales(P, S, in, lane);
     if (!warp_wait(P, S, &S.done[f], k & 1u, kWhereStorer)) break;
     if (lane == 0 && (P.flags & MK_FLAG_TRACE)) S.meta[f].t_sstart = gtimer();
     __syncwarp();
@@ -1680,14 +1730,14 @@ DEVI void storer(const KParams &P, const Smem &S, uint32_t epoch, int lane) {
       }
       __syncwarp();
     }
-    storer_epilogue(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);
+    storer_epilogue<Q8>(P, S, in, meta, S.res + (size_t)f * P.res_floats, lane, epoch);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.iempty[f]);
   }
 }
 
 // --------------------------------------------------------------- kernel ----
-template <bool TC>
+template <bool TC, bool Q8>
 DEVI void megakernel_body(const KParams &P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1795,9 +1845,9 @@ DEVI void megakernel_body(const KParams &P) {
     }
     __syncwarp();
   } else if (warp == 1) {
-    storer<TC>(P, S, epoch, lane);
+    storer<TC, Q8>(P, S, epoch, lane);
   } else {
-    compute<TC>(P, S, epoch, warp - 2, lane);
+    compute<TC, Q8>(P, S, epoch, warp - 2, lane);
   }
   __syncthreads();
   if (TC) {
@@ -1833,11 +1883,16 @@ DEVI void megakernel_body(const KParams &P) {
 // projections): the same persistent interpreter, compiled twice.
 extern "C" __global__ void __launch_bounds__(kThreads, 1)
     mk_megakernel(const __grid_constant__ KParams P) {
-  megakernel_body<false>(P);
+  megakernel_body<false, false>(P);
 }
 extern "C" __global__ void __launch_bounds__(kThreads, 1)
     mk_megakernel_tc(const __grid_constant__ KParams P) {
-  megakernel_body<true>(P);
+  megakernel_body<true, false>(P);
+}
+// Batch-1 plans with FP8 weights (MK_FLAG_FP8_WEIGHTS)
+extern "C" __global__ void __launch_bounds__(kThreads, 1)
+    mk_megakernel_q8(const __grid_constant__ KParams P) {
+  megakernel_body<false, true>(P);
 }
 
 // The multi-kernel path ends each step with this one-thread launch.
@@ -1893,10 +1948,67 @@ extern "C" __global__ void mk_retile_tc(uint8_t *dst, const uint8_t *src, const 
   }
 }
 
+// FP8 plans, step 1 of re-tiling a weight block: arena row k's scale, the
+// largest magnitude of source row map[k] over 448 (1 for a zero row), at
+// byte scaletab[k] of the block.  One warp per row.
+extern "C" __global__ void mk_row_scale(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                                        const uint64_t *scaletab, uint32_t nrows, uint32_t K) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = gridDim.x * (blockDim.x / 32);
+  for (uint32_t k = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; k < nrows; k += warps) {
+    const uint32_t srow = map ? (uint32_t)map[k] : k;
+    const uint16_t *row = reinterpret_cast<const uint16_t *>(src) + (uint64_t)srow * K;
+    float amax = 0.f;
+    for (uint32_t c = lane; c < K; c += 32) amax = fmaxf(amax, fabsf(bf1(row[c])));
+    amax = warp_max(amax);
+    if (lane == 0)
+      *reinterpret_cast<float *>(dst + scaletab[k]) = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+}
+
+// Step 2: the codes.  Eight columns per thread: code = E4M3 of w / scale
+// (the division correctly rounded in float, the conversion to nearest even
+// and saturating), written at the columns' place in their item (SW bytes
+// per item, ipp items per page), as the bf16 re-tiling places 2 SW bytes.
+extern "C" __global__ void mk_retile_q8(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                                        const uint64_t *rowtab, const uint64_t *scaletab,
+                                        uint32_t nrows, uint32_t K, uint32_t NS,
+                                        uint32_t item_bytes, uint32_t ipp, uint32_t page) {
+  const uint64_t per_row = K / 8;
+  const uint64_t total = (uint64_t)nrows * per_row;
+  const uint32_t SW = K / NS;
+  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (uint64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = (uint32_t)(i / per_row);
+    const uint32_t c = (uint32_t)(i % per_row) * 8;
+    const uint64_t rt = rowtab[k];
+    const uint32_t r = (uint32_t)(rt & 4095u);
+    const uint32_t item = r * NS + c / SW;
+    uint8_t *d = dst + (rt & ~(uint64_t)4095u) + (uint64_t)(item / ipp) * page +
+                 (uint64_t)(item % ipp) * item_bytes + c % SW;
+    const float sc = *reinterpret_cast<const float *>(dst + scaletab[k]);
+    const uint32_t srow = map ? (uint32_t)map[k] : k;
+    const uint4 w = *reinterpret_cast<const uint4 *>(src + ((uint64_t)srow * K + c) * 2);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t h = (ws[t / 2] >> (16 * (t % 2))) & 0xFFFFu;
+      const float v = __fdiv_rn(__uint_as_float(h << 16), sc);
+      const uint32_t q = (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+      out[t / 4] |= q << (8 * (t % 4));
+    }
+    *reinterpret_cast<uint2 *>(d) = make_uint2(out[0], out[1]);
+  }
+}
+
 // ---- host-side launch helpers (the kernels' host stubs live in this unit) ----
 cudaError_t set_megakernel_smem(uint32_t bytes) {
-  const cudaError_t e = cudaFuncSetAttribute(mk_megakernel_tc,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = cudaFuncSetAttribute(mk_megakernel_tc,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(mk_megakernel_q8, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bytes);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)bytes);
@@ -1914,8 +2026,27 @@ cudaError_t launch_megakernel(const KParams &P, uint32_t grid, bool cooperative,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cooperative ? 1 : 0;
-  return P.tc ? cudaLaunchKernelEx(&cfg, mk_megakernel_tc, P)
-              : cudaLaunchKernelEx(&cfg, mk_megakernel, P);
+  return P.tc    ? cudaLaunchKernelEx(&cfg, mk_megakernel_tc, P)
+         : P.fp8 ? cudaLaunchKernelEx(&cfg, mk_megakernel_q8, P)
+                 : cudaLaunchKernelEx(&cfg, mk_megakernel, P);
+}
+
+cudaError_t launch_row_scale(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             const uint64_t *scaletab, uint32_t nrows, uint32_t K,
+                             cudaStream_t stream) {
+  const uint32_t blocks = std::min<uint32_t>(65535u, (nrows + 7) / 8);
+  mk_row_scale<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, scaletab, nrows, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_retile_q8(uint8_t *dst, const uint8_t *src, const int32_t *map,
+                             const uint64_t *rowtab, const uint64_t *scaletab, uint32_t nrows,
+                             const OpGeom &g, uint32_t page, cudaStream_t stream) {
+  const uint64_t total = (uint64_t)nrows * g.K / 8;
+  const uint32_t blocks = (uint32_t)((total + 255) / 256 < 65535 ? (total + 255) / 256 : 65535);
+  mk_retile_q8<<<blocks ? blocks : 1, 256, 0, stream>>>(dst, src, map, rowtab, scaletab, nrows,
+                                                        g.K, g.NS, g.item_bytes, g.ipp, page);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_epoch_advance(uint32_t *ctrl, cudaStream_t stream) {

@@ -18,13 +18,14 @@
 
 namespace mk {
 
-static void geom_for(uint32_t K, uint32_t page, OpGeom &g) {
+// wb: bytes per weight (2 bf16, 1 FP8)
+static void geom_for(uint32_t K, uint32_t page, uint32_t wb, OpGeom &g) {
   uint32_t NS = (K + 256 * kMaxChunks - 1) / (256 * kMaxChunks);
   while (K % (NS * 256)) NS++;
   g.K = K;
   g.NS = NS;
   g.SW = K / NS;
-  g.item_bytes = 2 * g.SW;
+  g.item_bytes = wb * g.SW;
   g.ipp = page / g.item_bytes;
   g.nch = g.SW / 256;
 }
@@ -64,8 +65,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   const uint32_t page = c.page_bytes ? (uint32_t)c.page_bytes : c.batch > 16 ? 16384u : 32768u;
   if (page < 4096 || page > 65536 || page % 1024) REJECT("page_bytes must be a multiple of 1024 in 4096..65536");
 
+  if ((c.flags & MK_FLAG_FP8_WEIGHTS) && (c.batch != 1 || (c.flags & MK_FLAG_STREAM_B1)))
+    REJECT("FP8 weights: batch 1 plans on the shared page ring only");
+
   P = HostPlan();
   P.cfg = c;
+  P.fp8 = (c.flags & MK_FLAG_FP8_WEIGHTS) != 0;
   P.num_sms = num_sms;
   P.smem_limit = smem_limit;
   P.page_bytes = page;
@@ -80,11 +85,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // the item limit allows).  Units: rotation pairs for q/k/v rows (a pair is
   // one RoPE rotation); whole pages of rows for a tied LM head (its tiles
   // then are the plain embedding matrix); single outputs otherwise.
-  geom_for(H, page, P.geom[MK_OP_QKV]);
-  geom_for(QD, page, P.geom[MK_OP_OPROJ]);
-  geom_for(H, page, P.geom[MK_OP_GATEUP]);
-  geom_for(F, page, P.geom[MK_OP_DOWN]);
-  geom_for(H, page, P.geom[MK_OP_LMHEAD]);
+  const uint32_t wb = P.fp8 ? 1u : 2u;
+  geom_for(H, page, wb, P.geom[MK_OP_QKV]);
+  geom_for(QD, page, wb, P.geom[MK_OP_OPROJ]);
+  geom_for(H, page, wb, P.geom[MK_OP_GATEUP]);
+  geom_for(F, page, wb, P.geom[MK_OP_DOWN]);
+  geom_for(H, page, wb, P.geom[MK_OP_LMHEAD]);
   for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
     if (op == MK_OP_ATTN) continue;
     const OpGeom &g = P.geom[op];
@@ -111,7 +117,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   const uint32_t S_ = num_sms;
   const uint32_t lm_unit = [&] {
     const OpGeom &g = P.geom[MK_OP_LMHEAD];
-    if (!c.tie_embeddings || page % g.item_bytes) return 1u;
+    if (!c.tie_embeddings || P.fp8 || page % g.item_bytes) return 1u;
     uint32_t a = g.ipp, b2 = g.NS;
     while (b2) { const uint32_t t = a % b2; a = b2; b2 = t; }
     return g.ipp / a;  // rows per unit: a multiple of whole pages
@@ -167,6 +173,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   auto tile_pages = [&](int op, uint32_t wrows) {
     return cdiv((uint64_t)wrows * P.geom[op].NS, P.geom[op].ipp);
   };
+  // arena bytes of a batch-1 tile: its pages, then (FP8 plans) one float
+  // scale per row, padded so the next tile stays 4096-aligned
+  auto tile_span = [&](int op, uint32_t wrows) {
+    return (uint64_t)tile_pages(op, wrows) * page +
+           (P.fp8 ? align_up((uint64_t)wrows * 4, 4096) : 0);
+  };
   uint32_t tile_items_max = 0;
   for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
     for (uint32_t n : P.tiles[op])
@@ -177,6 +189,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     if (op == MK_OP_ATTN) continue;
     std::vector<uint64_t> &rt = P.rowtab[op];
     rt.clear();
+    P.scaletab[op].clear();
     uint64_t toff = 0;
     const int reps = op == MK_OP_QKV ? nkv : 1;
     for (int g = 0; g < reps; ++g)
@@ -192,7 +205,10 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
           continue;
         }
         for (uint32_t r = 0; r < w; ++r) rt.push_back(toff | r);
-        toff += (uint64_t)tile_pages(op, w) * page;
+        if (P.fp8)
+          for (uint32_t r = 0; r < w; ++r)
+            P.scaletab[op].push_back(toff + (uint64_t)tile_pages(op, w) * page + 4ull * r);
+        toff += tile_span(op, w);
       }
     P.block_bytes[op] = toff;
   }
@@ -268,6 +284,12 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   // with work
   uint32_t rel_deal = take(P.tc ? kMaxDealChunks * 8 + (kMaxDealChunks + 1) * 4 : 0, 16);
   uint32_t rel_rbuf = take(P.res_floats * 4, 16);  // storer's prefetched residuals
+  // FP8 plans: the storer's copy of the current tile's row scales
+  uint32_t wsc_floats = 0;
+  if (P.fp8)
+    for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op)
+      for (uint32_t n : P.tiles[op]) wsc_floats = std::max(wsc_floats, wrows_of(op, n));
+  uint32_t rel_wsc = take(wsc_floats * 4, 16);
   // staged GEMV input (normalised x, or the attention output) and attention scores
   uint32_t xs_floats = std::max<uint32_t>(H, QD);
   if (P.tc)  // the MMA's B operand, one page's columns (kc x N bf16) per ring slot
@@ -322,6 +344,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   P.off_misc = ring + rel_misc;
   P.off_deal = ring + rel_deal;
   P.off_rbuf = ring + rel_rbuf;
+  P.off_wsc = ring + rel_wsc;
   P.off_xs = ring + rel_xs;
   P.off_bars = ring + rel_bars;
   P.smem_total = ring + fixed;
@@ -352,7 +375,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     bool plain = page % g.item_bytes == 0;
     const std::vector<uint32_t> &t = P.tiles[MK_OP_LMHEAD];
     for (size_t i = 0; i + 1 < t.size(); ++i) plain = plain && (t[i] * g.NS) % g.ipp == 0;
-    P.embed_alias = c.tie_embeddings && plain && !P.tc && !P.stream;
+    P.embed_alias = c.tie_embeddings && plain && !P.tc && !P.stream && !P.fp8;
   }
   if (!P.embed_alias) {
     P.off_embed = off;
@@ -393,7 +416,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
   auto emit_tile = [&](uint8_t op, mk_instr in) {
     const OpGeom &g = P.geom[op];
     const uint32_t wrows = wrows_of(op, in.nrows);
-    P.weight_bytes += (uint64_t)wrows * g.K * 2;
+    P.weight_bytes += P.fp8 ? (uint64_t)wrows * (g.K + 4) : (uint64_t)wrows * g.K * 2;
     if (P.stream) {  // items of the tile back to back, (slice, row) order
       in.npages = 0;
       in.wofs = off;
@@ -405,7 +428,7 @@ int build_plan(const mk_config &cfg, uint32_t num_sms, uint32_t smem_limit, Host
     if (!P.tc) {
       in.npages = tile_pages(op, wrows);
       in.wofs = off;
-      off += (uint64_t)in.npages * page;
+      off += tile_span(op, wrows);
       push(in);
       P.ctr_inc[in.sig_ctr]++;
       return;

@@ -31,6 +31,10 @@ struct HostPlan {
   uint32_t n_wait = 0, n_ctr = 0, lm_ctr = 0;
   uint32_t attn_chunk = 0, nchunk = 0, att_lmax = 0;
   bool tc = false;              // batch > 1: projections on tcgen05, split along K
+  bool fp8 = false;             // batch 1: FP8 weight codes, one scale per tile row after
+                                // the tile's pages
+  std::vector<uint64_t> scaletab[8];  // FP8 plans, per op: arena row -> byte offset of its
+                                      // scale in the op's block
   bool stream = false;          // batch 1: every compute warp streams its own weights
   uint32_t tmem_cols = 32;      // tensor-core plans: tensor-memory columns allocated
   bool att_grp = false;         // tensor-core plans, d = 64, <= 4 heads per group: every
@@ -43,6 +47,7 @@ struct HostPlan {
   uint32_t ring_pages = 0, page_bytes = 0, res_floats = 0;
   uint32_t off_bars = 0, off_fifo = 0, off_meta = 0, off_res = 0, off_att = 0, off_sat = 0,
            off_pos = 0, off_rope = 0, off_normr = 0, off_misc = 0, off_rbuf = 0, off_xs = 0, off_wring = 0, off_deal = 0,
+           off_wsc = 0,
            smem_total = 0;
   uint32_t fault_instr = 0xFFFFFFFFu;
 };

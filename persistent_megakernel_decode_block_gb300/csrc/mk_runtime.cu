@@ -204,6 +204,7 @@ static int setup_device(mk_plan_s *p) {
   P.tc_nb = (int32_t)H.tc_nb;
   P.stream = H.stream ? 1 : 0;
   P.att_grp = H.att_grp ? 1 : 0;
+  P.fp8 = H.fp8 ? 1 : 0;
   P.tmem_cols = H.tmem_cols;
   P.wnb = H.wnb;
   P.off_wring = H.off_wring;
@@ -244,6 +245,7 @@ static int setup_device(mk_plan_s *p) {
   P.off_deal = H.off_deal;
   P.off_rbuf = H.off_rbuf;
   P.off_xs = H.off_xs;
+  P.off_wsc = H.off_wsc;
   P.smem_total = H.smem_total;
   return MK_OK;
 }
@@ -320,7 +322,7 @@ MK_API int mk_plan_info(mk_plan_t p, mk_plan_info_t *info) {
   info->arena_bytes = H.arena_bytes;
   info->weight_bytes = H.weight_bytes;
   info->warp_ring_slots = H.stream ? H.wnb : 0u;
-  info->kernel = H.stream ? 2u : H.tc ? 1u : 0u;
+  info->kernel = H.stream ? 2u : H.tc ? 1u : H.fp8 ? 3u : 0u;
   return MK_OK;
 }
 
@@ -379,25 +381,35 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
   stage_elems = std::max(stage_elems, V * H_);
   uint8_t *stage = nullptr;
   if (dalloc(&stage, stage_elems * 2) != MK_OK) return MK_ERR_NOMEM;
-  // the planner's row tables (arena row -> tile offset | row in tile), one per op
+  // the planner's row tables (arena row -> tile offset | row in tile), one per op,
+  // and for FP8 plans, after them, the row-scale tables (arena row -> scale offset)
   size_t rt_rows = 0, rt_at[8] = {};
   for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD; ++op) {
     rt_at[op] = rt_rows;
     rt_rows += H.rowtab[op].size();
   }
   uint64_t *rowtab = nullptr;
-  if (dalloc(&rowtab, rt_rows) != MK_OK) {
+  if (dalloc(&rowtab, H.fp8 ? 2 * rt_rows : rt_rows) != MK_OK) {
     cudaFree(stage);
     return MK_ERR_NOMEM;
   }
+  uint64_t *scaletab = rowtab + rt_rows;
   int rc = MK_OK;
-  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD && rc == MK_OK; ++op)
+  for (int op = MK_OP_QKV; op <= MK_OP_LMHEAD && rc == MK_OK; ++op) {
     if (!H.rowtab[op].empty() &&
         cudaMemcpy(rowtab + rt_at[op], H.rowtab[op].data(), H.rowtab[op].size() * 8,
                    cudaMemcpyHostToDevice) != cudaSuccess) {
       (void)cudaGetLastError();
       rc = MK_ERR_CUDA;
     }
+    if (H.fp8 && rc == MK_OK &&
+        (H.scaletab[op].size() != H.rowtab[op].size() ||
+         cudaMemcpy(scaletab + rt_at[op], H.scaletab[op].data(), H.scaletab[op].size() * 8,
+                    cudaMemcpyHostToDevice) != cudaSuccess)) {
+      (void)cudaGetLastError();
+      rc = MK_ERR_CUDA;
+    }
+  }
   const uint32_t pg = H.page_bytes;
   uint8_t *A = p->d_arena;
   auto norm_dst = [&](int idx) { return A + H.off_norms + (size_t)idx * H_ * 2; };
@@ -408,6 +420,12 @@ MK_API int mk_load_weights(mk_plan_t p, const mk_weights *w, void *stream) {
     } else if (H.stream) {
       if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
       e = launch_retile_stream(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], s);
+    } else if (H.fp8) {  // row scales first, then the codes (same stream)
+      if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
+      e = launch_row_scale(dst, stage, map, scaletab + rt_at[op], rows, H.geom[op].K, s);
+      if (e == cudaSuccess)
+        e = launch_retile_q8(dst, stage, map, rowtab + rt_at[op], scaletab + rt_at[op], rows,
+                             H.geom[op], pg, s);
     } else {
       if (rows != H.rowtab[op].size()) return MK_ERR_CONFIG;
       e = launch_retile(dst, stage, map, rowtab + rt_at[op], rows, H.geom[op], pg, s);

@@ -22,6 +22,7 @@ for _c, _n in ERRORS.items():
 MK_OP_QKV, MK_OP_ATTN, MK_OP_OPROJ, MK_OP_GATEUP, MK_OP_DOWN, MK_OP_LMHEAD = 1, 2, 3, 4, 5, 6
 MK_NO_COUNTER = 0xFFFFFFFF
 MK_FLAG_TRACE, MK_FLAG_HOST_ONLY, MK_FLAG_FAULT_WAIT, MK_FLAG_STREAM_B1 = 1, 2, 4, 8
+MK_FLAG_FP8_WEIGHTS = 0x10
 MK_SCHED_DYNAMIC, MK_SCHED_STATIC, MK_SCHED_HYBRID = 0, 1, 2
 MK_LIST_ATTN = 0x80000000  # hybrid lists: entry MK_LIST_ATTN | l = layer l's attention queue
 

@@ -20,7 +20,9 @@ def to_dev(a):
 
 class Setup:
     def __init__(self, name, seed=0, steps=None, sched=mk.MK_SCHED_DYNAMIC, flags=0, tie=None,
-                 with_oracle=True, timeout_us=0, ctx=None, mctx=None, **plan_kw):
+                 with_oracle=True, timeout_us=0, ctx=None, mctx=None, fp8=False, **plan_kw):
+        """fp8: the plan streams FP8 weights (MK_FLAG_FP8_WEIGHTS) and the
+        oracle runs the same FP8 form of the weights."""
         w = WORKLOADS[name]
         self.name, self.seed, self.sched = name, seed, sched
         self.m = dict(w["model"])
@@ -34,8 +36,10 @@ class Setup:
         self.mctx = max_ctx(name, seed, self.steps) if mctx is None else int(mctx)
         self.weights = make_model(self.m, seed)
         self.k0, self.v0 = make_kv(self.m, self.B, self.mctx, self.ctx, seed)
-        self.oracle = (oracle.Model(self.m, self.weights, self.B, self.mctx, self.k0, self.v0)
-                       if with_oracle else None)
+        self.oracle = (oracle.Model(self.m, self.weights, self.B, self.mctx, self.k0, self.v0,
+                                    fp8=fp8) if with_oracle else None)
+        if fp8:
+            flags |= mk.MK_FLAG_FP8_WEIGHTS
         dev = {"embed": to_dev(self.weights["embed"]),
                "final_norm": to_dev(self.weights["final_norm"]),
                "lm_head": None if self.m["tie_embeddings"] else to_dev(self.weights["lm_head"]),

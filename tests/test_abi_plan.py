@@ -321,3 +321,57 @@ def test_without_a_gpu_planning_on_the_device_fails_cleanly():
     with pytest.raises(mk.MkError) as e:
         mk.mk_plan(mk.make_config(w["model"], 1, 128))
     assert e.value.code == mk.MK_ERR_DEVICE
+
+
+@pytest.mark.parametrize("name", [n for n in ORDER if WORKLOADS[n]["batch"] == 1])
+def test_fp8_weight_plans(name):
+    """FP8 weights: the counter graph replays as for bf16; every weight is one
+    byte plus one 4-byte scale per output row; a tile's pages hold 1-byte
+    items (ipp = page / SW), followed in the arena by its row scales; the
+    plan runs on its own kernel instantiation."""
+    w = WORKLOADS[name]
+    p = host_plan(name, flags=mk.MK_FLAG_FP8_WEIGHTS)
+    b = host_plan(name)
+    try:
+        info, binfo = mk.mk_plan_info(p), mk.mk_plan_info(b)
+        assert info["kernel"] == 3 and binfo["kernel"] == 0
+        rec, raw, inc = mk.mk_plan_tables(p)
+        off, idx = mk.mk_plan_lists(p)
+        want = oracle.replay(raw, info["n_instr"], info["n_counters"], w["model"], w["batch"],
+                             info["n_blocks"], off, idx)
+        assert np.array_equal(inc, want)
+        assert np.array_equal(inc, mk.mk_plan_tables(b)[2])
+        m = w["model"]
+        H, F, V, L = m["hidden"], m["ffn_dim"], m["vocab"], m["n_layers"]
+        QD, KD = m["n_q_heads"] * m["head_dim"], m["n_kv_heads"] * m["head_dim"]
+        rows = L * ((QD + 2 * KD) + H + 2 * F + H) + V
+        per_layer = (QD + 2 * KD) * H + H * QD + 2 * F * H + H * F
+        assert info["weight_bytes"] == L * per_layer + V * H + 4 * rows
+        page = info["page_bytes"]
+        brec = mk.mk_plan_tables(b)[0]
+        for op, K in ((mk.MK_OP_QKV, H), (mk.MK_OP_OPROJ, QD), (mk.MK_OP_GATEUP, H),
+                      (mk.MK_OP_DOWN, F), (mk.MK_OP_LMHEAD, H)):
+            NS = -(-K // 1024)
+            while K % (NS * 256):
+                NS += 1
+            ipp = page // (K // NS)
+            t = rec[rec["op"] == op]
+            wrows = t["nrows"].astype(np.int64) * (2 if op == mk.MK_OP_GATEUP else 1)
+            assert np.array_equal(t["npages"], (wrows * NS + ipp - 1) // ipp)
+            assert (t["npages"] <= brec[brec["op"] == op]["npages"]).all()
+            # scales follow the pages; the next tile starts 4096-aligned
+            ends = t["wofs"] + t["npages"].astype(np.uint64) * page + wrows.astype(np.uint64) * 4
+            assert (t["wofs"] % 4096 == 0).all() and (ends[:-1] <= t["wofs"][1:]).all()
+    finally:
+        mk.mk_destroy(p)
+        mk.mk_destroy(b)
+
+
+@pytest.mark.parametrize("batch, flags", [(8, 0), (1, mk.MK_FLAG_STREAM_B1)])
+def test_fp8_weights_rejected_outside_batch_one_ring_plans(batch, flags):
+    m = WORKLOADS["tiny"]["model"]
+    cfg = mk.make_config(m, batch, 128, num_sms=152,
+                         flags=mk.MK_FLAG_HOST_ONLY | mk.MK_FLAG_FP8_WEIGHTS | flags)
+    with pytest.raises(mk.MkError) as e:
+        mk.mk_plan(cfg)
+    assert e.value.code == mk.MK_ERR_CONFIG
