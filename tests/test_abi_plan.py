@@ -313,6 +313,18 @@ def test_record_layout_matches_header():
         "nchunk": 40, "npages": 44, "wofs": 48, "phase": 56, "reserved": 60}
 
 
+def test_binding_constants_match_the_header():
+    # every MK_ constant the binding defines has the header's value
+    text = open(HEADER).read()
+    defs = {m.group(1): int(m.group(2), 0) for m in
+            re.finditer(r"#define\s+(MK_\w+)\s+(-?(?:0x[0-9a-fA-F]+|\d+))u?\b", text)}
+    names = [n for n in dir(mk) if n.startswith(("MK_FLAG_", "MK_SCHED_", "MK_OP_", "MK_LIST_"))
+             and isinstance(getattr(mk, n), int)]
+    assert len(names) >= 15
+    for n in names:
+        assert n in defs and defs[n] == getattr(mk, n), n
+
+
 def test_without_a_gpu_planning_on_the_device_fails_cleanly():
     import torch
     if torch.cuda.is_available():
