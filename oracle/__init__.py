@@ -6,9 +6,9 @@ A plain, slow, single-threaded fp64 C restatement of a Llama-style decode step
 leg may import this package.  It never imports the CUDA library and shares no
 code with it.
 
-Parity pins: every function is pinned by tests/test_oracle_pins.py and
-tests/test_replay_pins.py against closed forms, invariants, brute force and
-independent library routines.
+Parity pins: every function is pinned by tests/test_oracle_pins.py,
+tests/test_fp8_pins.py and tests/test_replay_pins.py against closed forms,
+invariants, brute force and independent library routines.
 """
 import ctypes
 import os

@@ -18,7 +18,10 @@
  * Precision: every intermediate is an IEEE double.  Weights and the KV cache
  * are bf16 (their storage type); a key or value written to the cache is
  * rounded to bf16 (round to nearest even) and read back rounded, as the
- * storage type dictates.
+ * storage type dictates.  The FP8 form of the weights (« Résumé exécutif »,
+ * "Les six leviers", names lower precision as a lever but no format) is read
+ * as E4M3 codes with one float scale per output row; or_quantize_rows
+ * derives it from the bf16 weights and or_matvec_q8 multiplies with it.
  */
 #include <math.h>
 #include <stdint.h>
